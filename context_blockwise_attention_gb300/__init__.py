@@ -1,0 +1,35 @@
+"""Per-rank context-parallel blockwise attention for GB300 (sm_103a).
+
+Python binding of ``libcpattn.so`` (C ABI in ``include/cpattn.h``).  The binding only checks and
+marshals arguments; every step of the computation runs in the library's CUDA kernels.  PyTorch
+is used for device memory and streams.  The shared library is loaded on first use and a missing
+or unloadable library raises -- there is no CPU fallback.
+"""
+
+from .api import (  # noqa: F401
+    CpError,
+    PosMap,
+    shard_layout,
+    sub_chunk_map,
+    partial_attn,
+    merge_partials,
+    ulysses_reshard,
+    library_path,
+    load_library,
+    version,
+    visible_pairs,
+)
+
+__all__ = [
+    "CpError",
+    "PosMap",
+    "shard_layout",
+    "sub_chunk_map",
+    "partial_attn",
+    "merge_partials",
+    "ulysses_reshard",
+    "library_path",
+    "load_library",
+    "version",
+    "visible_pairs",
+]

@@ -1,0 +1,185 @@
+/*
+ * cpattn.h -- C ABI of the per-rank context-parallel (CP) attention library (libcpattn.so).
+ *
+ * One CP rank's attention work on one GPU: which global token positions a rank holds, blockwise
+ * attention of the rank's query shard against one KV chunk at a time (chunks may arrive in any
+ * order) producing an (O, LSE) partial, the order-independent merge of partials into exact
+ * softmax attention, and the Ulysses sequence <-> head reshard.  CP ranks are logical shards;
+ * nothing here communicates between processes or GPUs.
+ *
+ * Sources (pages cited by title and section):
+ *   [FCP]     "FCP: from a fixed ring to a free topology" (lqnn.cn/news/264049)
+ *   [PCP/DCP] "PCP and DCP sequence parallelism guide" (hmyw.cn/news/122838)
+ *   [ZigZag]  "Zig-Zag Ring Attention" article (intelliparadigm.com, article 2133809)
+ *   [Halo]    "Halo context parallelism (CP + Ulysses attention)" (sheratonhq.com/news/191935)
+ *
+ * Conventions shared by every call:
+ *   - Tensors are token-major, batch 1: [tokens, heads, head_dim], contiguous, head_dim fastest.
+ *   - Global positions are affine per shard: pos(i) = base + stride * i, stride >= 1.
+ *   - All device pointers are caller-owned device memory; the library allocates no device memory
+ *     and keeps no state between calls.  Host pointer arrays are read during the call only.
+ *   - Every call is asynchronous on `stream` (0 = legacy default stream).  Argument checks run on
+ *     the host before anything is launched; a rejected call launches nothing.
+ *   - On a non-OK status, cp_last_error() returns a message for the calling thread.
+ */
+#ifndef CPATTN_H
+#define CPATTN_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CP_ABI_VERSION 1
+/* Largest number of partials one cp_merge_partials call accepts. */
+#define CP_MAX_PARTIALS 128
+
+typedef enum {
+  CP_OK = 0,
+  CP_ERR_INVALID_ARG = 1, /* rejected on the host; nothing launched                     */
+  CP_ERR_UNSUPPORTED = 2, /* device is not sm_103 (GB300) or the shape is not supported  */
+  CP_ERR_CUDA = 3,        /* a CUDA runtime/driver call or a launch failed               */
+  CP_ERR_TIMEOUT = 4      /* a bounded in-kernel wait expired (reported via *status)     */
+} cp_status;
+
+typedef enum { CP_LAYOUT_CONTIGUOUS = 0, CP_LAYOUT_STRIDED = 1 } cp_layout;
+typedef enum { CP_F32 = 0, CP_BF16 = 1 } cp_dtype;
+
+/* Global position of local token i: base + stride * i. */
+typedef struct {
+  int64_t base;
+  int64_t stride;
+} cp_posmap;
+
+/*
+ * cp_shard_layout -- which global tokens rank `rank` of `cp` holds.
+ *   [PCP/DCP] section 3.5 (split_sequence_for_cp): contiguous block starting at rank*seq_len/cp,
+ *             seq_len must divide by cp; positions stay global.
+ *   [ZigZag]  section 4.2: strided assignment, rank r holds r, r+cp, r+2cp, ...
+ * Arguments:
+ *   seq_len, cp, rank   sequence length (> 0), CP size (> 0), rank in [0, cp).
+ *   kind                CP_LAYOUT_CONTIGUOUS (base = rank*seq_len/cp, stride 1) or
+ *                       CP_LAYOUT_STRIDED    (base = rank,             stride cp).
+ *   map_out             host pointer, required: receives the affine map.
+ *   dev_positions_out   device int32 [seq_len/cp] or NULL; filled with pos(i) on `stream`
+ *                       (requires seq_len <= INT32_MAX).
+ * Errors: CP_ERR_INVALID_ARG when seq_len % cp != 0, rank out of range, map_out NULL, or an
+ *         unknown kind.  CP_ERR_CUDA if the fill kernel fails to launch.
+ */
+cp_status cp_shard_layout(int64_t seq_len, int32_t cp, int32_t rank, int32_t kind,
+                          cp_posmap* map_out, int32_t* dev_positions_out, cudaStream_t stream);
+
+/* Flags for cp_attn_desc.flags. */
+#define CP_FLAG_KV_DESCENDING 0x1 /* visit the chunk's KV tiles last-to-first (same result)   */
+#define CP_FLAG_TEST_STALL 0x100  /* test only: block 0 waits on a barrier nobody arrives on; */
+                                  /* its bounded wait expires, *status gets CP_ERR_TIMEOUT.   */
+
+/*
+ * Partial attention of one query shard against one KV chunk.
+ *   [FCP] section 3.3: scores = q . k^T / sqrt(head_dim); running max and running sum with
+ *   online-softmax rescaling over KV blocks; output = acc / running_sum.  The result does not
+ *   depend on the order in which chunks (or the tiles inside a chunk) are visited.
+ * Output is the normalised partial: O = softmax-weighted sum of the chunk's visible V rows and
+ * LSE = natural-log sum of exp(scores) over those keys.  A query row with no visible key in the
+ * chunk gets O = 0 and LSE = -inf.
+ * Fields:
+ *   q         device [sq, hq, d]  (in_dtype)
+ *   k, v      device [skv, hkv, d] (in_dtype)
+ *   in_dtype  CP_F32 (fp32 CUDA-core path) or CP_BF16 (tensor-core path, fp32 accumulation)
+ *   o         device [sq, hq, d]  (o_dtype: CP_F32, or CP_BF16 when this partial is final)
+ *   lse       device fp32 [sq, hq]
+ *   sq, skv   token counts (>= 0); hq, hkv head counts, hq % hkv == 0; Q head h reads KV head
+ *             h / (hq/hkv) ([Halo] native GQA, contiguous groups).  d in {64, 128}.
+ *   causal    1: key visible iff kv_pos(j) <= q_pos(i) (global positions, self included)
+ *   scale     softmax scale; 0 means 1/sqrt(d)
+ *   q_pos, kv_pos  affine position maps of the query shard and of the chunk
+ *   status    device int32 or NULL: set to CP_ERR_TIMEOUT | (site << 8) if a bounded wait
+ *             inside the kernel expires (the kernel then returns early; outputs undefined).
+ *             The caller zeroes it; read it after synchronising.
+ *   flags     CP_FLAG_* bits
+ *   wait_timeout_ms  limit of each in-kernel wait; 0 means 2000 ms
+ * Errors: CP_ERR_INVALID_ARG (null pointers, d not 64/128, hq % hkv, stride < 1, bad dtype,
+ * pointers not 16-byte aligned), CP_ERR_UNSUPPORTED (device not sm_103), CP_ERR_CUDA.
+ */
+typedef struct {
+  const void* q;
+  const void* k;
+  const void* v;
+  int32_t in_dtype;
+  int32_t o_dtype;
+  void* o;
+  float* lse;
+  int64_t sq;
+  int64_t skv;
+  int32_t hq;
+  int32_t hkv;
+  int32_t d;
+  int32_t causal;
+  float scale;
+  int32_t flags;
+  cp_posmap q_pos;
+  cp_posmap kv_pos;
+  int32_t* status;
+  int32_t wait_timeout_ms;
+  int32_t reserved;
+} cp_attn_desc;
+
+cp_status cp_partial_attn(const cp_attn_desc* desc, cudaStream_t stream);
+
+/*
+ * Merge n partials of the same query rows into exact attention.
+ *   [PCP/DCP] sections 2.3 and 4.2 (global_softmax): global max first, then exponentials
+ *   against it and their global sum, then normalise.  In (O, LSE) form:
+ *     M = max_i LSE_i;  w_i = exp(LSE_i - M);  O = sum_i w_i O_i / sum_i w_i;
+ *     LSE = M + ln sum_i w_i.
+ *   A partial with LSE_i = -inf contributes nothing and its O_i row is not read; if all are
+ *   -inf the result is O = 0, LSE = -inf.  The result does not depend on the order of parts.
+ * Arguments:
+ *   n          1 <= n <= CP_MAX_PARTIALS
+ *   o_parts    host array of n device pointers, each fp32 [sq, h, d]
+ *   lse_parts  host array of n device pointers, each fp32 [sq, h]
+ *   sq, h, d   rows, heads, head_dim (d % 4 == 0, d <= 256)
+ *   o_out      device [sq, h, d] in out_dtype (CP_F32 or CP_BF16, round-to-nearest-even)
+ *   lse_out    device fp32 [sq, h], or NULL to skip
+ * Errors: CP_ERR_INVALID_ARG (n out of range, null or unaligned pointers, bad sizes),
+ *         CP_ERR_CUDA.
+ */
+cp_status cp_merge_partials(int32_t n, const float* const* o_parts, const float* const* lse_parts,
+                            int64_t sq, int32_t h, int32_t d, void* o_out, int32_t out_dtype,
+                            float* lse_out, cudaStream_t stream);
+
+/*
+ * Ulysses reshard between sequence-sharded and head-sharded layouts, as a local permutation.
+ *   [Halo] "Ulysses attention": each rank holds S/cp tokens of all heads; the exchange gives
+ *   rank r all S tokens of heads [r*H/cp, (r+1)*H/cp); Q once, fused K|V once, O back.
+ *     dir 0 (seq -> head): out[t*cp + r][pos_s(i), j, :] = in[t*cp + s][i, r*H_t/cp + j, :]
+ *     dir 1 (head -> seq): out[t*cp + s][i, r*H_t/cp + j, :] = in[t*cp + r][pos_s(i), j, :]
+ *   where pos_s is shard s's layout (cp_shard_layout) and t indexes the tensors of one call.
+ * Arguments:
+ *   dir        0 or 1
+ *   cp         number of ranks (>= 1); seq_len % cp == 0
+ *   n_tensors  1..4 tensors moved in one launch (e.g. 2 for fused K|V)
+ *   heads      host array [n_tensors]: full head count H_t of each tensor; H_t % cp == 0
+ *   d          head_dim; (H_t/cp) * d * sizeof(dtype) must be a multiple of 16 bytes
+ *   dtype      CP_F32 or CP_BF16
+ *   layout     cp_layout of the sequence shards
+ *   in, out    host arrays [n_tensors*cp] of device pointers (16-byte aligned), shapes above
+ * Bit-exact copy.  Errors: CP_ERR_INVALID_ARG, CP_ERR_CUDA.
+ */
+cp_status cp_ulysses_reshard(int32_t dir, int32_t cp, int64_t seq_len, int32_t n_tensors,
+                             const int32_t* heads, int32_t d, int32_t dtype, int32_t layout,
+                             const void* const* in, void* const* out, cudaStream_t stream);
+
+/* Message for the calling thread's last non-OK status ("" if none).  Valid until the next call. */
+const char* cp_last_error(void);
+
+/* CP_ABI_VERSION of the loaded library. */
+int32_t cp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPATTN_H */
