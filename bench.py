@@ -1,0 +1,558 @@
+"""Benchmark of the per-rank context-parallel attention hot path on one GB300.
+
+One step = the whole path for one workload: the query rank's shard layout (positions filled on
+the device), a partial attention per KV chunk in the seeded arrival order, and the merge of the
+partials (workloads 1, 2, 3, 5); or, for the Ulysses workload 4, the seq->head reshard of Q and
+of fused K|V, full-sequence attention per head-rank and the head->seq reshard of O.
+
+Default workload (N=1): 2 -- causal bf16 GQA 32/8, D=128, S=32768, CP=8 strided, rank 7's 4096
+queries against the 8 KV chunks in a seeded random order.
+
+Prints one JSON line.  ``value`` is causal-adjusted attention TFLOP/s over the device-timed
+step (FLOPs = 4 * D * Hq * exact visible (q, k) pairs); ``e2e`` is the same metric through the
+C ABI with host buffers (pinned host -> device copies of the step's inputs and the device ->
+host read of its outputs inside the timed region).  ``--impl reference`` times the CPU oracle on
+a bounded sample of the same workload instead.
+
+Multi-GPU: the path does not need a collective.  Under torchrun each GPU simulates a different
+CP rank of the same workload (GPU i takes query rank cp-1-i); ranks only meet at a barrier
+around the timed region, and rank 0 reports the max time over ranks.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "causal-adjusted attention TFLOP/s and % bf16 roofline; merge/reshard HBM GB/s"
+L2_FLUSH_BYTES = 512 << 20  # > 129 MB of L2
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm": float(d["hbm_gbs"]), "bf16": float(d["bf16_tflops"]),
+                "bf16_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ----------------------------------------------------------------------------- workloads
+
+class Step:
+    """Inputs resident on the device plus the launch sequence of one step."""
+
+    def __init__(self, cfg, device, query_rank=None, layout=None, host_copy=False):
+        import context_blockwise_attention_gb300 as cpa
+        from context_blockwise_attention_gb300 import workloads as wl
+        self.cpa, self.wl = cpa, wl
+        self.w = w = wl.WORKLOADS[cfg]
+        self.cfg = cfg
+        self.device = device
+        self.layout = layout or w.layout
+        self.flops = 0
+        self.merge_bytes = 0
+        self.reshard_bytes = 0
+        self.launches = 0
+        self.attn_calls = []      # list of (kwargs) for partial_attn
+        self.merges = []          # list of (o_parts, l_parts, o_out, l_out)
+        self.host_inputs = []     # (host pinned, device) pairs copied in e2e mode
+        self.host_outputs = []    # (device, host pinned) pairs read back in e2e mode
+        if cfg == 4:
+            self._build_ulysses()
+        else:
+            ranks = [query_rank] if query_rank is not None else (
+                [w.query_rank] if w.query_rank >= 0 else list(range(w.cp)))
+            self._build_ranks(ranks)
+        if host_copy:
+            self.host_inputs = [(t.cpu().pin_memory(), t) for t in self._input_tensors]
+            self.host_outputs = [(t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True))
+                                 for t in self._output_tensors]
+
+    def _build_ranks(self, ranks):
+        cpa, wl, w = self.cpa, self.wl, self.w
+        dev = self.device
+        dt = w.torch_dtype
+        o_dtype = torch.float32
+        final_dtype = torch.float32 if w.dtype == "f32" else torch.bfloat16
+        kv = {}
+        self._input_tensors = []
+        self._output_tensors = []
+        self.pos_bufs = []
+        for r in sorted({c for c in range(w.cp)}):
+            k = wl.shard_tensor(w, "k", r, device=dev)
+            v = wl.shard_tensor(w, "v", r, device=dev)
+            kv[r] = (k, v)
+            self._input_tensors += [k, v]
+        self.rank_plans = []
+        for qr in ranks:
+            qmap = cpa.shard_layout(w.seq_len, w.cp, qr, self.layout)
+            q = wl.shard_tensor(w, "q", qr, device=dev)
+            self._input_tensors.append(q)
+            self.pos_bufs.append((qr, torch.empty(w.local_len, dtype=torch.int32, device=dev)))
+            order = wl.arrival_order(w.n_chunks, w.order_seed + 17 * qr)
+            o_parts, l_parts = [], []
+            for ci in order:
+                src, sub = divmod(int(ci), w.chunks_per_shard)
+                kmap = cpa.sub_chunk_map(cpa.shard_layout(w.seq_len, w.cp, src, self.layout), sub,
+                                         w.chunk_len)
+                n_vis = cpa.visible_pairs(qmap, w.local_len, kmap, w.chunk_len, w.causal)
+                if w.causal and n_vis == 0:
+                    continue  # chunk entirely in the future of this shard: never issued
+                k, v = kv[src]
+                ks = k[sub * w.chunk_len:(sub + 1) * w.chunk_len]
+                vs = v[sub * w.chunk_len:(sub + 1) * w.chunk_len]
+                o = torch.empty((w.local_len, w.hq, w.d), dtype=o_dtype, device=dev)
+                l = torch.empty((w.local_len, w.hq), dtype=torch.float32, device=dev)
+                self.attn_calls.append(dict(q=q, k=ks, v=vs, q_pos=qmap, kv_pos=kmap,
+                                            causal=w.causal, o=o, lse=l))
+                self.flops += 4 * w.d * w.hq * n_vis
+                o_parts.append(o)
+                l_parts.append(l)
+                fr = cpa.finite_rows(qmap, w.local_len, kmap, w.chunk_len, w.causal)
+                self.merge_bytes += w.local_len * w.hq * 4 + fr * w.hq * w.d * 4
+            out = torch.empty((w.local_len, w.hq, w.d), dtype=final_dtype, device=dev)
+            lse = torch.empty((w.local_len, w.hq), dtype=torch.float32, device=dev)
+            self.merge_bytes += out.numel() * out.element_size() + lse.numel() * 4
+            self.merges.append((o_parts, l_parts, out, lse))
+            self._output_tensors += [out, lse]
+            self.rank_plans.append((qr, qmap, q, order))
+
+    def _build_ulysses(self):
+        cpa, wl, w = self.cpa, self.wl, self.w
+        dev = self.device
+        cp, S = w.cp, w.seq_len
+        self.qs = [wl.shard_tensor(w, "q", r, device=dev) for r in range(cp)]
+        self.ks = [wl.shard_tensor(w, "k", r, device=dev) for r in range(cp)]
+        self.vs = [wl.shard_tensor(w, "v", r, device=dev) for r in range(cp)]
+        self._input_tensors = self.qs + self.ks + self.vs
+        hl, kl = w.hq // cp, w.hkv // cp
+        self.yq = [torch.empty((S, hl, w.d), dtype=torch.bfloat16, device=dev) for _ in range(cp)]
+        self.yk = [torch.empty((S, kl, w.d), dtype=torch.bfloat16, device=dev) for _ in range(cp)]
+        self.yv = [torch.empty((S, kl, w.d), dtype=torch.bfloat16, device=dev) for _ in range(cp)]
+        self.yo = [torch.empty((S, hl, w.d), dtype=torch.bfloat16, device=dev) for _ in range(cp)]
+        self.ylse = [torch.empty((S, hl), dtype=torch.float32, device=dev) for _ in range(cp)]
+        self.xo = [torch.empty((S // cp, w.hq, w.d), dtype=torch.bfloat16, device=dev)
+                   for _ in range(cp)]
+        self._output_tensors = self.xo
+        full = cpa.PosMap(0, 1)
+        n_vis = cpa.visible_pairs(full, S, full, S, True)
+        for r in range(cp):
+            self.attn_calls.append(dict(q=self.yq[r], k=self.yk[r], v=self.yv[r], q_pos=full,
+                                        kv_pos=full, causal=True, o=self.yo[r], lse=self.ylse[r]))
+            self.flops += 4 * w.d * hl * n_vis
+        el = 2
+        self.reshard_bytes = 2 * el * w.d * S * (w.hq + 2 * w.hkv + w.hq)
+        self.pos_bufs = []
+
+    # ----------------------------------------------------------------- launch sequence
+    def run(self, timers=None):
+        """Launch one step on the current stream; optional timers record per-kernel events."""
+        cpa, w = self.cpa, self.w
+        stream = torch.cuda.current_stream()
+        n = 0
+
+        def ev():
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(stream)
+            return e
+        if self.cfg == 4:
+            t0 = ev() if timers is not None else None
+            cpa.ulysses_reshard("seq_to_head", [self.qs], w.cp, w.seq_len, w.layout, out=[self.yq])
+            cpa.ulysses_reshard("seq_to_head", [self.ks, self.vs], w.cp, w.seq_len, w.layout,
+                                out=[self.yk, self.yv])
+            t1 = ev() if timers is not None else None
+            for kw in self.attn_calls:
+                cpa.partial_attn(**kw)
+            t2 = ev() if timers is not None else None
+            cpa.ulysses_reshard("head_to_seq", [self.yo], w.cp, w.seq_len, w.layout, out=[self.xo])
+            t3 = ev() if timers is not None else None
+            n = 3 + len(self.attn_calls)
+            if timers is not None:
+                timers["reshard"].append((t0, t1))
+                timers["reshard"].append((t2, t3))
+                timers["attn"].append((t1, t2))
+            return n
+        for qr, buf in self.pos_bufs:
+            lib = cpa.load_library()
+            import ctypes
+            from context_blockwise_attention_gb300 import api
+            m = api._PosMap()
+            st = lib.cp_shard_layout(w.seq_len, w.cp, qr, api._LAYOUTS[self.layout],
+                                     ctypes.byref(m), ctypes.c_void_p(buf.data_ptr()),
+                                     ctypes.c_void_p(stream.cuda_stream))
+            api._check(st)
+            n += 1
+        t1 = ev() if timers is not None else None
+        for kw in self.attn_calls:
+            cpa.partial_attn(**kw)
+            n += 1
+        t2 = ev() if timers is not None else None
+        for o_parts, l_parts, out, lse in self.merges:
+            cpa.merge_partials(o_parts, l_parts, o=out, lse=lse)
+            n += 1
+        t3 = ev() if timers is not None else None
+        if timers is not None:
+            timers["attn"].append((t1, t2))
+            timers["merge"].append((t2, t3))
+        return n
+
+    def run_e2e(self):
+        """Host -> device copies of the inputs, the step, device -> host copies of the outputs."""
+        for h, d in self.host_inputs:
+            d.copy_(h, non_blocking=True)
+        n = self.run()
+        for d, h in self.host_outputs:
+            h.copy_(d, non_blocking=True)
+        return n
+
+    @property
+    def h2d_bytes(self):
+        return sum(h.numel() * h.element_size() for h, _ in self.host_inputs)
+
+    @property
+    def d2h_bytes(self):
+        return sum(h.numel() * h.element_size() for _, h in self.host_outputs)
+
+
+# ----------------------------------------------------------------------------- measurement
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _profile_traffic(kernel_file, workload_key):
+    """dram bytes per launch of the dominant kernel from the committed ncu summary, or None if
+    the kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(workload_key)
+        with open(kernel_file, "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()[:16]
+        if rec and rec.get("kernel_sha256_16") == h:
+            return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def _blas_threads():
+    try:
+        import ctypes
+        with open("/proc/self/maps") as f:
+            libs = {l.split()[-1] for l in f if "openblas" in l.lower() and ".so" in l}
+        for lib in libs:
+            h = ctypes.CDLL(lib)
+            for sym in ("openblas_get_num_threads64_", "openblas_get_num_threads"):
+                fn = getattr(h, sym, None)
+                if fn is not None:
+                    return int(fn())
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+def oracle_sample(cfg, rows_per_rank, seed=5, layout=None):
+    """Time the CPU oracle on a bounded sample of the workload: for ``rows_per_rank`` seeded
+    query rows, every chunk's partial then the merge.  Returns (seconds, causal-adjusted FLOPs,
+    description)."""
+    import oracle
+    from context_blockwise_attention_gb300 import workloads as wl
+    w = wl.WORKLOADS[cfg]
+    layout = layout or w.layout
+    ranks = [w.query_rank] if w.query_rank >= 0 else [w.cp - 1]
+    flops = 0
+    t = 0.0
+    if cfg == 4:
+        # full-sequence attention of head-rank 0 on sampled rows (the reshard is a copy)
+        S = w.seq_len
+        hl, kl = w.hq // w.cp, w.hkv // w.cp
+        q = wl.normal((rows_per_rank, hl, w.d), torch.bfloat16, 11, 0.5)
+        k = wl.normal((S, kl, w.d), torch.bfloat16, 12, 0.5)
+        v = wl.normal((S, kl, w.d), torch.bfloat16, 13, 0.5)
+        rows = np.sort(np.random.default_rng(seed).choice(S, rows_per_rank, replace=False))
+        t0 = time.perf_counter()
+        oracle.attention(q, k, v, rows, np.arange(S), causal=True)
+        t = time.perf_counter() - t0
+        flops = 4 * w.d * hl * int((rows + 1).sum())
+        return t, flops, f"{rows_per_rank} query rows x {hl} heads vs {S} keys (head-rank 0)"
+    for qr in ranks:
+        qpos = oracle.shard_positions(w.seq_len, w.cp, qr, layout)
+        rows = wl.sample_rows(w.local_len, rows_per_rank, seed)
+        q = wl.shard_tensor(w, "q", qr, tokens=w.local_len)[rows]
+        parts = []
+        for c in range(w.n_chunks):
+            src, sub = divmod(c, w.chunks_per_shard)
+            k = wl.shard_tensor(w, "k", src)[sub * w.chunk_len:(sub + 1) * w.chunk_len]
+            v = wl.shard_tensor(w, "v", src)[sub * w.chunk_len:(sub + 1) * w.chunk_len]
+            kpos = oracle.sub_chunk_positions(oracle.shard_positions(w.seq_len, w.cp, src, layout),
+                                              sub, w.chunk_len)
+            t0 = time.perf_counter()
+            parts.append(oracle.attention(q, k, v, qpos[rows], kpos, causal=w.causal))
+            t += time.perf_counter() - t0
+            flops += 4 * w.d * w.hq * oracle.visible_pair_count(qpos[rows], kpos, w.causal)
+        t0 = time.perf_counter()
+        oracle.merge([p[0] for p in parts], [p[1] for p in parts])
+        t += time.perf_counter() - t0
+    return t, flops, (f"{rows_per_rank} seeded query rows of rank {ranks[0]} x {w.hq} heads "
+                      f"against all {w.n_chunks} chunks, then the merge")
+
+
+def _config_dict(w, layout, extra):
+    d = {"workload": f"cfg{w.index}: {w.name}", "layout": layout, "seq_len": w.seq_len,
+         "cp": w.cp, "hq": w.hq, "hkv": w.hkv, "head_dim": w.d, "causal": w.causal,
+         "chunks": w.n_chunks, "chunk_tokens": w.chunk_len,
+         "l2": "flushed (512 MiB write) before every timed step"}
+    d.update(extra)
+    return d
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    from context_blockwise_attention_gb300 import workloads as wl
+    w = wl.WORKLOADS[args.config]
+    if world > 1 and rank != 0:
+        return
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        oracle_sample(args.config, max(1, rows // 4))
+    times, fl = [], 0
+    desc = ""
+    for _ in range(args.steps):
+        t, fl, desc = oracle_sample(args.config, rows)
+        times.append(t)
+    tmean = sum(times) / len(times)
+    value = fl / tmean / 1e12
+    cores = _blas_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": tmean * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": _config_dict(w, args.layout or w.layout, {"sample_rows": rows}),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu(args):
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    import context_blockwise_attention_gb300 as cpa
+    from context_blockwise_attention_gb300 import workloads as wl
+    cpa.load_library()
+    w = wl.WORKLOADS[args.config]
+    layout = args.layout or w.layout
+    qr = None
+    if w.query_rank >= 0:
+        qr = (w.cp - 1 - rank) % w.cp
+    step = Step(args.config, dev, query_rank=qr, layout=layout, host_copy=True)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step.run()
+    barrier()
+
+    # ---- device-timed steps (inputs resident), L2 flushed before each
+    timers = {"attn": [], "merge": [], "reshard": []}
+    sampler = ClockSampler(local)
+    sampler.start()
+    step_ms, launches = [], 0
+    stream = torch.cuda.current_stream()
+    for _ in range(args.steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        launches += step.run(timers)
+        b.record(stream)
+        torch.cuda.synchronize()
+        step_ms.append(a.elapsed_time(b))
+    barrier()
+    clocks = sampler.stop()
+    total_ms = sum(step_ms)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * step.flops / (ms_per_step * 1e-3) / 1e12
+
+    def seg(name):
+        xs = [s.elapsed_time(e) for s, e in timers[name]]
+        return sum(xs) / len(xs) if xs else None
+    attn_ms = seg("attn")
+    merge_ms = seg("merge")
+    reshard_ms = seg("reshard")
+
+    # ---- end to end through the C ABI with host buffers
+    for _ in range(2):
+        step.run_e2e()
+    barrier()
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step.run_e2e()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    e2e_total = sum(e2e_ms)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    e2e_value = world * step.flops / (e2e_total / args.steps * 1e-3) / 1e12
+
+    peaks = _peaks()
+    n_attn = len(step.attn_calls)
+    achieved = step.flops / (attn_ms * 1e-3) / 1e12
+    traffic = _profile_traffic(os.path.join(ROOT, "context_blockwise_attention_gb300", "csrc",
+                                            "attn_tc.cu"), f"cfg{args.config}")
+    roofline = {"bound": "tensor", "kernel": "attn_tc_kernel", "achieved": achieved,
+                "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16"],
+                "peak_source": f"{peaks['source']} bf16 dense (burst)",
+                "frac_of_sustained": achieved / peaks["bf16_sustained"],
+                "launches_per_step": n_attn,
+                "traffic": traffic}
+    extra = {"attn_ms_per_step": attn_ms, "attn_tflops": achieved,
+             "step_flop": step.flops, "query_rank": qr}
+    if merge_ms:
+        gbs = step.merge_bytes / (merge_ms * 1e-3) / 1e9
+        extra["merge"] = {"ms": merge_ms, "GB/s": gbs, "frac": gbs / peaks["hbm"],
+                          "bytes": step.merge_bytes}
+    if reshard_ms:
+        gbs = step.reshard_bytes / (reshard_ms * 1e-3) / 1e9
+        extra["reshard"] = {"ms": reshard_ms, "GB/s": gbs, "frac": gbs / peaks["hbm"],
+                            "bytes": step.reshard_bytes}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        t, fl, desc = oracle_sample(args.config, args.ref_rows)
+        cpu = {"value": fl / t / 1e12, "unit": "TFLOP/s", "cores": _blas_threads(),
+               "kind": "oracle", "sample": desc, "seconds": t}
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16" if w.dtype == "bf16" else "f32",
+                "data": "synthetic (seeded N(0,1) inputs; no dataset or weights)",
+                "config": _config_dict(w, layout, {"parallelism": f"replicas x{world}"}),
+                "e2e": {"value": e2e_value, "unit": "TFLOP/s",
+                        "h2d_bytes_per_step": step.h2d_bytes,
+                        "d2h_bytes_per_step": step.d2h_bytes,
+                        "ms_per_step": e2e_total / args.steps},
+                "gpu_launches": launches,
+                "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks, **extra}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--layout", default=None, choices=[None, "contiguous", "strided"])
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--ref-rows", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl != "reference":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -18,6 +18,7 @@ from .api import (  # noqa: F401
     load_library,
     version,
     visible_pairs,
+    finite_rows,
 )
 
 __all__ = [
@@ -32,4 +33,5 @@ __all__ = [
     "load_library",
     "version",
     "visible_pairs",
+    "finite_rows",
 ]

@@ -1,0 +1,282 @@
+"""ctypes binding of libcpattn.so (C ABI in include/cpattn.h).
+
+Argument checking and marshalling only: tensors are passed as ``data_ptr()`` on the caller's
+current CUDA stream.  Each function raises CpError on a non-OK status, with the library's own
+message.  The library must be built (``__graft_entry__.build()``); there is no fallback.
+"""
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+from . import build as _build
+
+CP_OK, CP_ERR_INVALID_ARG, CP_ERR_UNSUPPORTED, CP_ERR_CUDA, CP_ERR_TIMEOUT = range(5)
+CP_LAYOUT_CONTIGUOUS, CP_LAYOUT_STRIDED = 0, 1
+CP_F32, CP_BF16 = 0, 1
+CP_FLAG_KV_DESCENDING = 0x1
+CP_FLAG_TEST_STALL = 0x100
+CP_MAX_PARTIALS = 128
+
+_LAYOUTS = {"contiguous": CP_LAYOUT_CONTIGUOUS, "strided": CP_LAYOUT_STRIDED,
+            CP_LAYOUT_CONTIGUOUS: CP_LAYOUT_CONTIGUOUS, CP_LAYOUT_STRIDED: CP_LAYOUT_STRIDED}
+
+
+class CpError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__(f"status {status}: {message}")
+        self.status = status
+
+
+class _PosMap(ctypes.Structure):
+    _fields_ = [("base", ctypes.c_int64), ("stride", ctypes.c_int64)]
+
+
+class _AttnDesc(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("in_dtype", ctypes.c_int32), ("o_dtype", ctypes.c_int32),
+        ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("sq", ctypes.c_int64), ("skv", ctypes.c_int64),
+        ("hq", ctypes.c_int32), ("hkv", ctypes.c_int32), ("d", ctypes.c_int32),
+        ("causal", ctypes.c_int32), ("scale", ctypes.c_float), ("flags", ctypes.c_int32),
+        ("q_pos", _PosMap), ("kv_pos", _PosMap),
+        ("status", ctypes.c_void_p), ("wait_timeout_ms", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+    ]
+
+
+@dataclass(frozen=True)
+class PosMap:
+    """Affine global positions of a shard or chunk: pos(i) = base + stride * i."""
+    base: int
+    stride: int
+
+
+_lib = None
+
+
+def library_path():
+    return _build.LIB
+
+
+def load_library():
+    """Load libcpattn.so once and declare its signatures; raise if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise CpError(CP_ERR_UNSUPPORTED, f"{path} is not built; run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    lib.cp_version.restype = i32
+    lib.cp_version.argtypes = []
+    lib.cp_last_error.restype = ctypes.c_char_p
+    lib.cp_last_error.argtypes = []
+    lib.cp_shard_layout.restype = i32
+    lib.cp_shard_layout.argtypes = [i64, i32, i32, i32, ctypes.POINTER(_PosMap), vp, vp]
+    lib.cp_partial_attn.restype = i32
+    lib.cp_partial_attn.argtypes = [ctypes.POINTER(_AttnDesc), vp]
+    lib.cp_merge_partials.restype = i32
+    lib.cp_merge_partials.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), i64, i32, i32,
+                                      vp, i32, vp, vp]
+    lib.cp_ulysses_reshard.restype = i32
+    lib.cp_ulysses_reshard.argtypes = [i32, i32, i64, i32, ctypes.POINTER(i32), i32, i32, i32,
+                                       ctypes.POINTER(vp), ctypes.POINTER(vp), vp]
+    _lib = lib
+    return lib
+
+
+def _check(status):
+    if status != CP_OK:
+        msg = load_library().cp_last_error().decode(errors="replace")
+        raise CpError(status, msg)
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _dtype_code(dt):
+    if dt == torch.float32:
+        return CP_F32
+    if dt == torch.bfloat16:
+        return CP_BF16
+    raise CpError(CP_ERR_INVALID_ARG, f"unsupported dtype {dt}")
+
+
+def _need_cuda(t, name):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise CpError(CP_ERR_INVALID_ARG, f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise CpError(CP_ERR_INVALID_ARG, f"{name} must be contiguous")
+
+
+def version():
+    return load_library().cp_version()
+
+
+def shard_layout(seq_len, cp, rank, kind="contiguous", positions=False, device=None, stream=None):
+    """Affine position map of rank ``rank``; with ``positions=True`` also an int32 CUDA tensor
+    of the positions, filled by the library's kernel."""
+    lib = load_library()
+    m = _PosMap()
+    out = None
+    ptr = None
+    if positions:
+        if seq_len % cp != 0 or cp <= 0:
+            _check(lib.cp_shard_layout(seq_len, cp, rank, _LAYOUTS.get(kind, -1), ctypes.byref(m),
+                                       None, None))
+        device = device or torch.device("cuda", torch.cuda.current_device())
+        out = torch.empty(seq_len // cp, dtype=torch.int32, device=device)
+        ptr = ctypes.c_void_p(out.data_ptr())
+    _check(lib.cp_shard_layout(int(seq_len), int(cp), int(rank), _LAYOUTS.get(kind, -1),
+                               ctypes.byref(m), ptr, _stream(stream) if positions else None))
+    pm = PosMap(m.base, m.stride)
+    return (pm, out) if positions else pm
+
+
+def sub_chunk_map(shard: PosMap, index: int, length: int) -> PosMap:
+    """Map of local rows [index*length, (index+1)*length) of a shard."""
+    return PosMap(shard.base + shard.stride * index * length, shard.stride)
+
+
+def partial_attn(q, k, v, q_pos: PosMap, kv_pos: PosMap, causal=True, scale=0.0, o=None,
+                 lse=None, o_dtype=None, flags=0, status=None, wait_timeout_ms=0, stream=None):
+    """(O, LSE) partial of query shard ``q`` [Sq, Hq, D] against one KV chunk [Skv, Hkv, D]."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need_cuda(t, n)
+    if q.dim() != 3 or k.dim() != 3 or v.shape != k.shape:
+        raise CpError(CP_ERR_INVALID_ARG, "q must be [Sq, Hq, D]; k and v [Skv, Hkv, D]")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise CpError(CP_ERR_INVALID_ARG, "q, k, v must share a dtype")
+    sq, hq, d = q.shape
+    skv, hkv, dk = k.shape
+    if dk != d:
+        raise CpError(CP_ERR_INVALID_ARG, "head_dim mismatch")
+    if o is None:
+        o = torch.empty((sq, hq, d), dtype=o_dtype or torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((sq, hq), dtype=torch.float32, device=q.device)
+    _need_cuda(o, "o")
+    _need_cuda(lse, "lse")
+    if tuple(o.shape) != (sq, hq, d) or tuple(lse.shape) != (sq, hq) or lse.dtype != torch.float32:
+        raise CpError(CP_ERR_INVALID_ARG, "o must be [Sq, Hq, D]; lse fp32 [Sq, Hq]")
+    desc = _AttnDesc()
+    desc.q, desc.k, desc.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
+    desc.in_dtype = _dtype_code(q.dtype)
+    desc.o_dtype = _dtype_code(o.dtype)
+    desc.o, desc.lse = o.data_ptr(), lse.data_ptr()
+    desc.sq, desc.skv, desc.hq, desc.hkv, desc.d = sq, skv, hq, hkv, d
+    desc.causal = 1 if causal else 0
+    desc.scale = float(scale)
+    desc.flags = int(flags)
+    desc.q_pos = _PosMap(q_pos.base, q_pos.stride)
+    desc.kv_pos = _PosMap(kv_pos.base, kv_pos.stride)
+    if status is not None:
+        _need_cuda(status, "status")
+        if status.dtype != torch.int32:
+            raise CpError(CP_ERR_INVALID_ARG, "status must be int32")
+        desc.status = status.data_ptr()
+    desc.wait_timeout_ms = int(wait_timeout_ms)
+    _check(lib.cp_partial_attn(ctypes.byref(desc), _stream(stream)))
+    return o, lse
+
+
+def merge_partials(o_parts, lse_parts, out_dtype=torch.bfloat16, o=None, lse=None, stream=None):
+    """Exact attention from partials (lists of fp32 [Sq, H, D] and fp32 [Sq, H])."""
+    lib = load_library()
+    n = len(o_parts)
+    if n != len(lse_parts) or n < 1:
+        raise CpError(CP_ERR_INVALID_ARG, "need matching non-empty partial lists")
+    if n > CP_MAX_PARTIALS:
+        raise CpError(CP_ERR_INVALID_ARG, f"at most {CP_MAX_PARTIALS} partials")
+    sq, h, d = o_parts[0].shape
+    for x, y in zip(o_parts, lse_parts):
+        _need_cuda(x, "o part")
+        _need_cuda(y, "lse part")
+        if x.dtype != torch.float32 or y.dtype != torch.float32:
+            raise CpError(CP_ERR_INVALID_ARG, "partials must be fp32")
+        if tuple(x.shape) != (sq, h, d) or tuple(y.shape) != (sq, h):
+            raise CpError(CP_ERR_INVALID_ARG, "partials must share shape [Sq, H, D] / [Sq, H]")
+    if o is None:
+        o = torch.empty((sq, h, d), dtype=out_dtype, device=o_parts[0].device)
+    if lse is None:
+        lse = torch.empty((sq, h), dtype=torch.float32, device=o_parts[0].device)
+    _need_cuda(o, "o")
+    _need_cuda(lse, "lse")
+    arr_o = (ctypes.c_void_p * n)(*[x.data_ptr() for x in o_parts])
+    arr_l = (ctypes.c_void_p * n)(*[y.data_ptr() for y in lse_parts])
+    _check(lib.cp_merge_partials(n, arr_o, arr_l, sq, h, d, ctypes.c_void_p(o.data_ptr()),
+                                 _dtype_code(o.dtype), ctypes.c_void_p(lse.data_ptr()),
+                                 _stream(stream)))
+    return o, lse
+
+
+def ulysses_reshard(direction, tensors, cp, seq_len, layout="contiguous", out=None, stream=None):
+    """Reshard ``tensors`` (a list over tensor kinds, each a list of cp per-rank tensors).
+
+    direction "seq_to_head": inputs [S/cp, H_t, D] -> outputs [S, H_t/cp, D];
+    direction "head_to_seq": inputs [S, H_t/cp, D] -> outputs [S/cp, H_t, D].
+    Returns the outputs in the same nesting.
+    """
+    lib = load_library()
+    dirc = {"seq_to_head": 0, "head_to_seq": 1}[direction]
+    nt = len(tensors)
+    heads = []
+    outs = []
+    for t, per_rank in enumerate(tensors):
+        if len(per_rank) != cp:
+            raise CpError(CP_ERR_INVALID_ARG, "one tensor per rank expected")
+        x0 = per_rank[0]
+        d = x0.shape[2]
+        h_t = x0.shape[1] if dirc == 0 else x0.shape[1] * cp
+        heads.append(h_t)
+        for x in per_rank:
+            _need_cuda(x, "reshard input")
+        if out is not None:
+            outs.append(out[t])
+        elif dirc == 0:
+            outs.append([torch.empty((seq_len, h_t // cp, d), dtype=x0.dtype, device=x0.device)
+                         for _ in range(cp)])
+        else:
+            outs.append([torch.empty((seq_len // cp, h_t, d), dtype=x0.dtype, device=x0.device)
+                         for _ in range(cp)])
+    d = tensors[0][0].shape[2]
+    dtype = tensors[0][0].dtype
+    arr_in = (ctypes.c_void_p * (nt * cp))(*[x.data_ptr() for per in tensors for x in per])
+    arr_out = (ctypes.c_void_p * (nt * cp))(*[y.data_ptr() for per in outs for y in per])
+    arr_h = (ctypes.c_int32 * nt)(*heads)
+    _check(lib.cp_ulysses_reshard(dirc, cp, seq_len, nt, arr_h, d, _dtype_code(dtype),
+                                  _LAYOUTS[layout], arr_in, arr_out, _stream(stream)))
+    return outs
+
+
+def visible_pairs(q_map: PosMap, n_q: int, k_map: PosMap, n_k: int, causal=True) -> int:
+    """Exact count of (query, key) pairs with kv_pos <= q_pos (for FLOP accounting)."""
+    import numpy as np
+    if not causal:
+        return int(n_q) * int(n_k)
+    qp = q_map.base + q_map.stride * np.arange(n_q, dtype=np.int64)
+    cnt = np.where(qp < k_map.base, 0, (qp - k_map.base) // k_map.stride + 1)
+    return int(np.minimum(cnt, n_k).sum())
+
+
+def finite_rows(q_map: PosMap, n_q: int, k_map: PosMap, n_k: int, causal=True) -> int:
+    """Number of query rows that see at least one key of the chunk (rows whose partial LSE is
+    finite); used for the merge's algorithmic byte count."""
+    import numpy as np
+    if n_k == 0:
+        return 0
+    if not causal:
+        return int(n_q)
+    qp = q_map.base + q_map.stride * np.arange(n_q, dtype=np.int64)
+    return int((qp >= k_map.base).sum())

@@ -1,0 +1,579 @@
+// Partial attention for bf16 inputs on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// What it computes ("FCP: from a fixed ring to a free topology", section 3.3): for a query
+// block, visit KV blocks in any order; per block form scores q . k^T / sqrt(head_dim), update
+// the running maximum, rescale the accumulator and running sum by exp(old - new), add
+// exp(scores - new_max) @ V and its row sum; output = acc / running_sum.  The kernel emits the
+// normalised partial O and LSE = ln(sum exp(scores)) of one KV chunk; partials from different
+// chunks are combined by the merge kernel.
+//
+// How (GB300 design, not the pages'):
+//   * One CTA = two 128-row Q tiles (A, B) of one head.  KV tiles are 128 keys.
+//   * warp 0: TMA producer (Q once; K and V tiles through a ring of shared-memory stages,
+//     128-byte swizzled).  warp 1: allocates tensor memory and issues tcgen05.mma from one
+//     thread.  warps 4-7 / 8-11: softmax warpgroups for Q tiles A / B, one thread per row.
+//   * Tensor memory (512 columns): S_A, S_B (128 fp32 columns each), O_A, O_B (D columns).
+//     P (bf16) is written back over the first 64 columns of its S tile and fed to the PV
+//     product straight from tensor memory.
+//   * The tensor pipe runs QK_A(j), PV_B(j-1), QK_B(j), PV_A(j): each softmax warpgroup has two
+//     MMA slots to turn its S tile into P while the other tile keeps the tensor core busy.
+//   * Online softmax in base 2 with a lazy rescale: O and l are rescaled only when a row's
+//     maximum grows by more than 2^8; otherwise exponentials use the stale maximum.  The final
+//     O / l and LSE use that same reference, so the result is exact.
+//   * Causal visibility is by global position: key j is visible to query i iff
+//     kv_pos(j) <= q_pos(i).  KV tiles entirely in the future of the CTA's last row are never
+//     loaded or multiplied; only tiles that straddle the boundary (or the ragged end of the
+//     chunk) are masked element by element.
+//   * CTAs are ordered longest-first (the hardware block scheduler then balances the causal
+//     triangle), with the Q heads of one KV group adjacent so their K/V tiles are shared in L2.
+//   * Every mbarrier wait is bounded by %globaltimer; on expiry the kernel records
+//     CP_ERR_TIMEOUT in the caller's status word, every role leaves its loop, outstanding TMA
+//     loads and MMAs are drained and tensor memory is freed before the CTA exits.
+#include <math.h>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace cpattn {
+
+namespace {
+
+constexpr int kRows = 128;     // rows per Q tile
+constexpr int kKeys = 128;     // keys per KV tile
+constexpr int kThreads = 384;  // 12 warps
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+enum WaitSite : int {
+  kSiteQ = 1,
+  kSiteKFull = 2,
+  kSiteKEmpty = 3,
+  kSiteVFull = 4,
+  kSiteVEmpty = 5,
+  kSiteSFull = 6,
+  kSitePFull = 7,
+  kSiteOFinal = 8,
+  kSiteTest = 9,
+};
+
+struct TcParams {
+  void* o;
+  float* lse;
+  int32_t* status;
+  int64_t sq, skv;
+  int32_t hq, hkv, group;
+  int32_t n_pairs;
+  int32_t causal, o_bf16, descending, test_stall;
+  float scale_log2;
+  int64_t q_base, q_stride, k_base, k_stride;
+  int64_t timeout_ns;
+};
+
+template <int D>
+struct Layout {
+  static constexpr int kChunks = D / 64;             // 128-byte column chunks of a tile
+  static constexpr int kChunkBytes = 128 * 128;      // 128 rows x 128 bytes
+  static constexpr int kTileBytes = kRows * D * 2;   // bf16 tile
+  static constexpr int kStages = (D == 64) ? 4 : 2;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = 2 * kTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  // barriers: q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2],
+  //           o_final[2], never, drain
+  static constexpr int kNumBars = 1 + 4 * kStages + 6 + 2;
+  static constexpr int kOffCtl = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffCtl + 16;
+  static constexpr int kSmemLaunch = kBytes + 1024;  // slack for 1024-byte alignment
+};
+
+struct Bars {
+  uint32_t q_full;
+  uint32_t k_full, k_empty, v_full, v_empty;  // stage 0; +8 per stage
+  uint32_t s_full, p_full, o_final;           // tile A; +8 for tile B
+  uint32_t never, drain;
+};
+
+struct Ctl {
+  volatile int* abort;
+  int32_t* status;
+  int64_t timeout_ns;
+};
+
+__device__ __forceinline__ void raise_abort(const Ctl& c, int site) {
+  *c.abort = 1;
+  if (c.status != nullptr) atomicCAS(c.status, 0, CP_ERR_TIMEOUT | (site << 8));
+}
+
+// Waits for phase `parity` of `bar`; gives up (returns false) when the kernel is aborting or
+// when the wait exceeds the time limit, in which case it starts the abort itself.
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Ctl& c, int site) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0) {
+      if (*c.abort) return false;
+      if (static_cast<int64_t>(ptx::globaltimer() - t0) > c.timeout_ns) {
+        raise_abort(c, site);
+        return false;
+      }
+    }
+  }
+}
+
+// Teardown wait: ignores the abort flag (the copy or MMA must really finish) but stays bounded.
+__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, int64_t timeout_ns) {
+  const uint64_t t0 = ptx::globaltimer();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (static_cast<int64_t>(ptx::globaltimer() - t0) > timeout_ns) return;
+  }
+}
+
+__device__ __forceinline__ int64_t visible_keys(const TcParams& p, int64_t row) {
+  // keys j with k_base + k_stride * j <= q_pos(row), clipped to the chunk
+  const int64_t qp = p.q_base + p.q_stride * row;
+  if (qp < p.k_base) return 0;
+  const int64_t n = (qp - p.k_base) / p.k_stride + 1;
+  return n < p.skv ? n : p.skv;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tm_q,
+                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+  using L = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- the work unit: a pair of Q tiles of one head, longest first when causal
+  const int64_t u = blockIdx.x;
+  const int64_t pair = p.causal ? (p.n_pairs - 1 - u / p.hq) : (u / p.hq);
+  const int h = static_cast<int>(u % p.hq);
+  const int kvh = h / p.group;
+  const int64_t row0 = pair * (2 * kRows);
+  int64_t n_keys = p.skv;
+  if (p.causal) {
+    int64_t last = row0 + 2 * kRows - 1;
+    if (last > p.sq - 1) last = p.sq - 1;
+    n_keys = visible_keys(p, last);
+  }
+  const int n_tiles = static_cast<int>((n_keys + kKeys - 1) / kKeys);
+
+  Bars b;
+  b.q_full = sbase + L::kOffBar;
+  b.k_full = b.q_full + 8;
+  b.k_empty = b.k_full + 8 * L::kStages;
+  b.v_full = b.k_empty + 8 * L::kStages;
+  b.v_empty = b.v_full + 8 * L::kStages;
+  b.s_full = b.v_empty + 8 * L::kStages;
+  b.p_full = b.s_full + 16;
+  b.o_final = b.p_full + 16;
+  b.never = b.o_final + 16;
+  b.drain = b.never + 8;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffCtl);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffCtl + 4);
+  const Ctl ctl{abort_flag, p.status, p.timeout_ns};
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    ptx::mbar_init(b.q_full, 1);
+    for (int s = 0; s < L::kStages; ++s) {
+      ptx::mbar_init(b.k_full + 8 * s, 1);
+      ptx::mbar_init(b.k_empty + 8 * s, 1);
+      ptx::mbar_init(b.v_full + 8 * s, 1);
+      ptx::mbar_init(b.v_empty + 8 * s, 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      ptx::mbar_init(b.s_full + 8 * t, 1);
+      ptx::mbar_init(b.p_full + 8 * t, 4);
+      ptx::mbar_init(b.o_final + 8 * t, 1);
+    }
+    ptx::mbar_init(b.never, 1);
+    ptx::mbar_init(b.drain, 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const uint32_t sQ = sbase + L::kOffQ;
+  const uint32_t sK = sbase + L::kOffK;
+  const uint32_t sV = sbase + L::kOffV;
+
+  if (warp == 0) {
+    // ================================================================ TMA producer
+    if (lane == 0 && n_tiles > 0) {
+      ptx::tma_prefetch_desc(&tm_q);
+      ptx::tma_prefetch_desc(&tm_k);
+      ptx::tma_prefetch_desc(&tm_v);
+      ptx::mbar_arrive_expect_tx(b.q_full, 2 * L::kTileBytes);
+      for (int x = 0; x < 2; ++x)
+        for (int c = 0; c < L::kChunks; ++c)
+          ptx::tma_load_2d(sQ + x * L::kTileBytes + c * L::kChunkBytes, &tm_q, h * D + c * 64,
+                           static_cast<int32_t>(row0 + x * kRows), b.q_full);
+      int issued_k = 0, issued_v = 0;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int t = p.descending ? n_tiles - 1 - j : j;
+        const int st = j % L::kStages;
+        const uint32_t ph = (j / L::kStages) & 1;
+        if (!wait_bounded(b.k_empty + 8 * st, ph ^ 1, ctl, kSiteKEmpty)) break;
+        ptx::mbar_arrive_expect_tx(b.k_full + 8 * st, L::kTileBytes);
+        for (int c = 0; c < L::kChunks; ++c)
+          ptx::tma_load_2d(sK + st * L::kTileBytes + c * L::kChunkBytes, &tm_k, kvh * D + c * 64,
+                           t * kKeys, b.k_full + 8 * st);
+        issued_k = j + 1;
+        if (!wait_bounded(b.v_empty + 8 * st, ph ^ 1, ctl, kSiteVEmpty)) break;
+        ptx::mbar_arrive_expect_tx(b.v_full + 8 * st, L::kTileBytes);
+        for (int c = 0; c < L::kChunks; ++c)
+          ptx::tma_load_2d(sV + st * L::kTileBytes + c * L::kChunkBytes, &tm_v, kvh * D + c * 64,
+                           t * kKeys, b.v_full + 8 * st);
+        issued_v = j + 1;
+      }
+      if (*abort_flag) {
+        // copies in flight must land before the CTA's shared memory goes away
+        wait_drain(b.q_full, 0, p.timeout_ns);
+        for (int s = 0; s < L::kStages; ++s) {
+          const int last_k = ((issued_k - 1 - s) >= 0) ? issued_k - 1 - ((issued_k - 1 - s) % L::kStages) : -1;
+          if (last_k >= 0) wait_drain(b.k_full + 8 * s, (last_k / L::kStages) & 1, p.timeout_ns);
+          const int last_v = ((issued_v - 1 - s) >= 0) ? issued_v - 1 - ((issued_v - 1 - s) % L::kStages) : -1;
+          if (last_v >= 0) wait_drain(b.v_full + 8 * s, (last_v / L::kStages) & 1, p.timeout_ns);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(kRows, kKeys, 0, 0);
+      constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kRows, D, 0, 1);
+      const uint32_t tS[2] = {tmem + 0u, tmem + 128u};
+      const uint32_t tO[2] = {tmem + 256u, tmem + 384u};
+      bool ok = true;
+      if (p.test_stall && blockIdx.x == 0) ok = wait_bounded(b.never, 0, ctl, kSiteTest);
+      if (ok && n_tiles > 0) ok = wait_bounded(b.q_full, 0, ctl, kSiteQ);
+
+      auto issue_qk = [&](int x, int st) {
+        const uint32_t qa = sQ + x * L::kTileBytes;
+        const uint32_t ka = sK + st * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
+          ptx::mma_ss(tS[x], ptx::smem_desc_sw128(qa + off, 16, 1024),
+                      ptx::smem_desc_sw128(ka + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int x, int st, bool acc) {
+        const uint32_t va = sV + st * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          ptx::mma_ts(tO[x], tS[x] + kk * 8, ptx::smem_desc_sw128(va + kk * 2048, L::kChunkBytes, 1024),
+                      kIdescPV, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int st = j % L::kStages;
+        const uint32_t ph = (j / L::kStages) & 1;
+        if (!(ok = wait_bounded(b.k_full + 8 * st, ph, ctl, kSiteKFull))) break;
+        ptx::tc_fence_after();
+        issue_qk(0, st);
+        ptx::mma_commit(b.s_full);
+        if (j > 0) {
+          const int pst = (j - 1) % L::kStages;
+          if (!(ok = wait_bounded(b.p_full + 8, (j - 1) & 1, ctl, kSitePFull))) break;
+          ptx::tc_fence_after();
+          issue_pv(1, pst, j - 1 > 0);
+          ptx::mma_commit(b.v_empty + 8 * pst);
+        }
+        issue_qk(1, st);
+        ptx::mma_commit(b.s_full + 8);
+        ptx::mma_commit(b.k_empty + 8 * st);
+        if (!(ok = wait_bounded(b.v_full + 8 * st, ph, ctl, kSiteVFull))) break;
+        if (!(ok = wait_bounded(b.p_full, j & 1, ctl, kSitePFull))) break;
+        ptx::tc_fence_after();
+        issue_pv(0, st, j > 0);
+        if (j == n_tiles - 1) ptx::mma_commit(b.o_final);
+      }
+      if (ok && n_tiles > 0) {
+        const int j = n_tiles - 1;
+        const int st = j % L::kStages;
+        if ((ok = wait_bounded(b.p_full + 8, j & 1, ctl, kSitePFull))) {
+          ptx::tc_fence_after();
+          issue_pv(1, st, j > 0);
+          ptx::mma_commit(b.v_empty + 8 * st);
+          ptx::mma_commit(b.o_final + 8);
+        }
+      }
+      if (!ok) {
+        // every MMA issued so far must complete before tensor memory is released
+        ptx::mma_commit(b.drain);
+        wait_drain(b.drain, 0, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ================================================================ softmax warpgroups
+    const int x = (warp - 4) >> 2;           // 0: tile A, 1: tile B
+    const int wq = warp & 3;                 // lane quarter of tensor memory
+    const int r = wq * 32 + lane;            // row inside the tile
+    const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + x * 128u + lane_bits;
+    const uint32_t tO = tmem + 256u + x * 128u + lane_bits;
+    const int64_t tile_row0 = row0 + x * kRows;
+    const int64_t grow = tile_row0 + r;
+    const int64_t lim = p.causal ? visible_keys(p, grow) : p.skv;
+    const int64_t q_first = p.q_base + p.q_stride * tile_row0;
+    const float sl2 = p.scale_log2;
+
+    float m_ref = -INFINITY;  // running maximum (log2 units of scaled scores)
+    float l = 0.0f;           // running sum of 2^(x - m_ref)
+    bool ok = true;
+
+    for (int j = 0; j < n_tiles; ++j) {
+      const int t = p.descending ? n_tiles - 1 - j : j;
+      ok = wait_bounded(b.s_full + 8 * x, j & 1, ctl, kSiteSFull);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + c * 32, sr[c]);
+      ptx::tmem_wait_ld();
+
+      const int64_t k0 = static_cast<int64_t>(t) * kKeys;
+      const bool need_mask =
+          (k0 + kKeys > p.skv) || (p.causal && p.k_base + p.k_stride * (k0 + kKeys - 1) > q_first);
+      float mx = -INFINITY;
+      if (need_mask) {
+        const int64_t lim_local = lim - k0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float v = (c * 32 + e < lim_local) ? __uint_as_float(sr[c][e]) : -INFINITY;
+            sr[c][e] = __float_as_uint(v);
+            mx = fmaxf(mx, v);
+          }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[c][e]));
+      }
+      const float m_tile = mx * sl2;  // -inf stays -inf
+      bool rescale = false;
+      float factor = 1.0f;
+      if (m_ref == -INFINITY) {
+        m_ref = m_tile;  // first visible keys: O and l are still zero
+      } else if (m_tile > m_ref + kRescaleThreshold) {
+        rescale = true;
+        factor = ptx::ex2(m_ref - m_tile);
+        m_ref = m_tile;
+        l *= factor;
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          ptx::tmem_ld32(tO + c * 32, o);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
+          ptx::tmem_st32(tO + c * 32, o);
+        }
+      }
+      const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = ptx::ex2(fmaf(__uint_as_float(sr[c][2 * e]), sl2, -m_use));
+          const float p1 = ptx::ex2(fmaf(__uint_as_float(sr[c][2 * e + 1]), sl2, -m_use));
+          l += p0 + p1;
+          pk[e] = ptx::pack_bf16x2(p0, p1);
+        }
+        ptx::tmem_st16(tS + c * 16, pk);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(b.p_full + 8 * x);
+    }
+
+    // ---------------------------------------------------------------- epilogue
+    if (ok && n_tiles > 0) {
+      ok = wait_bounded(b.o_final + 8 * x, 0, ctl, kSiteOFinal);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) ptx::tc_fence_after();
+    }
+    if (ok) {
+      const bool has = (m_ref != -INFINITY) && (l > 0.0f);
+      const float inv = has ? 1.0f / l : 0.0f;
+      const bool row_ok = grow < p.sq;
+      const int64_t obase = (grow * p.hq + h) * static_cast<int64_t>(D);
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        if (n_tiles > 0) {
+          ptx::tmem_ld32(tO + c * 32, o);
+          ptx::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0u;
+        }
+        if (row_ok) {
+          if (p.o_bf16) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + obase + c * 32);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint4 w;
+              w.x = ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 0]) * inv, __uint_as_float(o[8 * q4 + 1]) * inv);
+              w.y = ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv, __uint_as_float(o[8 * q4 + 3]) * inv);
+              w.z = ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv, __uint_as_float(o[8 * q4 + 5]) * inv);
+              w.w = ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv, __uint_as_float(o[8 * q4 + 7]) * inv);
+              dst[q4] = w;
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + obase + c * 32);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+              dst[q4] = make_float4(__uint_as_float(o[4 * q4 + 0]) * inv, __uint_as_float(o[4 * q4 + 1]) * inv,
+                                    __uint_as_float(o[4 * q4 + 2]) * inv, __uint_as_float(o[4 * q4 + 3]) * inv);
+          }
+        }
+      }
+      if (row_ok)
+        p.lse[grow * p.hq + h] = has ? (m_ref * 0.69314718055994531f + logf(l)) : -INFINITY;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+// O = 0, LSE = -inf for every row (a chunk with no keys).
+__global__ void fill_empty_kernel(void* o, int o_bf16, float* lse, int64_t rows, int64_t row_elems) {
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t n = rows * row_elems;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += step) {
+    if (o_bf16)
+      static_cast<__nv_bfloat16*>(o)[i] = __float2bfloat16(0.0f);
+    else
+      static_cast<float*>(o)[i] = 0.0f;
+    if (i < rows) lse[i] = -INFINITY;
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 2-D map over a token-major bf16 tensor viewed as [tokens, heads*d]; box = 64 columns x 128 rows
+// with 128-byte swizzle (the canonical K-major / MN-major UMMA layout).
+bool make_map(CUtensorMap* m, const void* base, int64_t tokens, int64_t row_elems) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_elems), static_cast<cuuint64_t>(tokens)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_elems * 2)};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D>
+cp_status launch_tc(const TcParams& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                    int64_t grid, cudaStream_t s) {
+  constexpr int smem = Layout<D>::kSmemLaunch;
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attn_tc_kernel)");
+  attn_tc_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p, mq, mk, mv);
+  e = cudaGetLastError();
+  return e == cudaSuccess ? CP_OK : cuda_fail(e, "attn_tc_kernel launch");
+}
+
+}  // namespace
+
+cp_status launch_partial_attn_tc(const cp_attn_desc& d, float scale, int64_t timeout_ns, int /*num_sms*/,
+                                 cudaStream_t s) {
+  if (d.skv == 0) {
+    const int64_t n = d.sq * d.hq * d.d;
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    fill_empty_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(d.o, d.o_dtype == CP_BF16, d.lse,
+                                                                     d.sq * d.hq, d.d);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? CP_OK : cuda_fail(e, "fill_empty_kernel launch");
+  }
+  TcParams p;
+  p.o = d.o;
+  p.lse = d.lse;
+  p.status = d.status;
+  p.sq = d.sq;
+  p.skv = d.skv;
+  p.hq = d.hq;
+  p.hkv = d.hkv;
+  p.group = d.hq / d.hkv;
+  p.n_pairs = static_cast<int32_t>((d.sq + 2 * kRows - 1) / (2 * kRows));
+  p.causal = d.causal;
+  p.o_bf16 = d.o_dtype == CP_BF16;
+  p.descending = (d.flags & CP_FLAG_KV_DESCENDING) ? 1 : 0;
+  p.test_stall = (d.flags & CP_FLAG_TEST_STALL) ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.q_base = d.q_pos.base;
+  p.q_stride = d.q_pos.stride;
+  p.k_base = d.kv_pos.base;
+  p.k_stride = d.kv_pos.stride;
+  p.timeout_ns = timeout_ns;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, d.q, d.sq, int64_t(d.hq) * d.d) || !make_map(&mk, d.k, d.skv, int64_t(d.hkv) * d.d) ||
+      !make_map(&mv, d.v, d.skv, int64_t(d.hkv) * d.d)) {
+    set_error("cuTensorMapEncodeTiled failed (or the driver entry point is unavailable)");
+    return CP_ERR_CUDA;
+  }
+  const int64_t grid = static_cast<int64_t>(p.n_pairs) * d.hq;
+  if (grid > 0x7fffffff) {
+    set_error("partial attention grid too large");
+    return CP_ERR_INVALID_ARG;
+  }
+  if (d.d == 64) return launch_tc<64>(p, mq, mk, mv, grid, s);
+  return launch_tc<128>(p, mq, mk, mv, grid, s);
+}
+
+}  // namespace cpattn

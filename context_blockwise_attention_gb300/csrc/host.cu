@@ -1,0 +1,227 @@
+// C entry points of libcpattn.so: argument validation (host only, before any launch), device
+// check, dispatch to the kernels' launchers, and the per-thread error message.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace cpattn {
+
+static thread_local char g_err[512] = "";
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+void clear_error() { g_err[0] = '\0'; }
+
+cp_status cuda_fail(cudaError_t e, const char* what) {
+  set_error("%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+  return CP_ERR_CUDA;
+}
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+int g_dev_state[kMaxDevices];  // 0 unknown, 1 ok, 2 unsupported
+int g_dev_sms[kMaxDevices];
+int g_dev_cc[kMaxDevices];
+}  // namespace
+
+cp_status require_sm103(int* device_out, int* num_sms_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) {
+    set_error("device ordinal %d out of range", dev);
+    return CP_ERR_UNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_dev_state[dev] == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(major)");
+    if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(minor)");
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    g_dev_cc[dev] = major * 10 + minor;
+    g_dev_sms[dev] = sms;
+    g_dev_state[dev] = (major == 10 && minor == 3) ? 1 : 2;
+  }
+  if (g_dev_state[dev] != 1) {
+    set_error("device %d has compute capability %d.%d; this library is built for sm_103a (GB300)",
+              dev, g_dev_cc[dev] / 10, g_dev_cc[dev] % 10);
+    return CP_ERR_UNSUPPORTED;
+  }
+  if (device_out) *device_out = dev;
+  if (num_sms_out) *num_sms_out = g_dev_sms[dev];
+  return CP_OK;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int64_t dtype_size(int32_t t) { return t == CP_F32 ? 4 : (t == CP_BF16 ? 2 : 0); }
+
+}  // namespace cpattn
+
+using namespace cpattn;
+
+#define CP_INVALID(...)          \
+  do {                           \
+    cpattn::set_error(__VA_ARGS__); \
+    return CP_ERR_INVALID_ARG;   \
+  } while (0)
+
+CP_API int32_t cp_version(void) { return CP_ABI_VERSION; }
+
+CP_API const char* cp_last_error(void) { return cpattn::g_err; }
+
+CP_API cp_status cp_shard_layout(int64_t seq_len, int32_t cp, int32_t rank, int32_t kind,
+                                 cp_posmap* map_out, int32_t* dev_positions_out,
+                                 cudaStream_t stream) {
+  clear_error();
+  if (map_out == nullptr) CP_INVALID("cp_shard_layout: map_out is NULL");
+  if (seq_len <= 0) CP_INVALID("cp_shard_layout: seq_len must be positive (got %lld)", (long long)seq_len);
+  if (cp <= 0) CP_INVALID("cp_shard_layout: cp must be positive (got %d)", cp);
+  if (rank < 0 || rank >= cp) CP_INVALID("cp_shard_layout: rank %d not in [0, %d)", rank, cp);
+  if (seq_len % cp != 0)
+    CP_INVALID("cp_shard_layout: seq_len %lld is not a multiple of cp %d", (long long)seq_len, cp);
+  const int64_t local = seq_len / cp;
+  cp_posmap m;
+  if (kind == CP_LAYOUT_CONTIGUOUS) {
+    m.base = static_cast<int64_t>(rank) * local;
+    m.stride = 1;
+  } else if (kind == CP_LAYOUT_STRIDED) {
+    m.base = rank;
+    m.stride = cp;
+  } else {
+    CP_INVALID("cp_shard_layout: unknown layout kind %d", kind);
+  }
+  if (dev_positions_out != nullptr) {
+    if (seq_len > INT32_MAX) CP_INVALID("cp_shard_layout: int32 positions need seq_len <= INT32_MAX");
+    cp_status st = require_sm103(nullptr, nullptr);
+    if (st != CP_OK) return st;
+    st = launch_fill_positions(dev_positions_out, local, m.base, m.stride, stream);
+    if (st != CP_OK) return st;
+  }
+  *map_out = m;
+  return CP_OK;
+}
+
+CP_API cp_status cp_partial_attn(const cp_attn_desc* desc, cudaStream_t stream) {
+  clear_error();
+  if (desc == nullptr) CP_INVALID("cp_partial_attn: desc is NULL");
+  const cp_attn_desc& d = *desc;
+  if (d.in_dtype != CP_F32 && d.in_dtype != CP_BF16)
+    CP_INVALID("cp_partial_attn: in_dtype %d is not CP_F32 or CP_BF16", d.in_dtype);
+  if (d.o_dtype != CP_F32 && d.o_dtype != CP_BF16)
+    CP_INVALID("cp_partial_attn: o_dtype %d is not CP_F32 or CP_BF16", d.o_dtype);
+  if (d.sq < 0 || d.skv < 0) CP_INVALID("cp_partial_attn: negative token count");
+  if (d.sq > (int64_t(1) << 31) - 256 || d.skv > (int64_t(1) << 31) - 256)
+    CP_INVALID("cp_partial_attn: token counts must stay below 2^31");
+  if (d.hq <= 0 || d.hkv <= 0) CP_INVALID("cp_partial_attn: head counts must be positive");
+  if (d.hq % d.hkv != 0) CP_INVALID("cp_partial_attn: hq %d is not a multiple of hkv %d", d.hq, d.hkv);
+  if (d.d != 64 && d.d != 128) CP_INVALID("cp_partial_attn: head_dim %d not in {64, 128}", d.d);
+  if (d.causal != 0 && d.causal != 1) CP_INVALID("cp_partial_attn: causal must be 0 or 1");
+  if (d.q_pos.stride < 1 || d.kv_pos.stride < 1)
+    CP_INVALID("cp_partial_attn: position strides must be >= 1");
+  if (d.q_pos.base < 0 || d.kv_pos.base < 0) CP_INVALID("cp_partial_attn: positions must be >= 0");
+  // positions must stay inside int64 comfortably and inside int32 for the kernels' arithmetic
+  {
+    const double qmax = double(d.q_pos.base) + double(d.q_pos.stride) * double(d.sq);
+    const double kmax = double(d.kv_pos.base) + double(d.kv_pos.stride) * double(d.skv);
+    if (qmax > 2.0e9 || kmax > 2.0e9) CP_INVALID("cp_partial_attn: global positions exceed 2e9");
+  }
+  if (!(d.scale >= 0.0f) || isinf(d.scale)) CP_INVALID("cp_partial_attn: scale must be finite and >= 0");
+  if (d.flags & ~(CP_FLAG_KV_DESCENDING | CP_FLAG_TEST_STALL))
+    CP_INVALID("cp_partial_attn: unknown flag bits 0x%x", d.flags);
+  if (d.wait_timeout_ms < 0) CP_INVALID("cp_partial_attn: wait_timeout_ms must be >= 0");
+  if (d.sq > 0) {
+    if (d.q == nullptr || d.o == nullptr || d.lse == nullptr)
+      CP_INVALID("cp_partial_attn: q, o and lse must not be NULL");
+    if (!aligned16(d.q) || !aligned16(d.o) || (reinterpret_cast<uintptr_t>(d.lse) & 3u))
+      CP_INVALID("cp_partial_attn: q and o must be 16-byte aligned, lse 4-byte aligned");
+  }
+  if (d.skv > 0 && d.sq > 0) {
+    if (d.k == nullptr || d.v == nullptr) CP_INVALID("cp_partial_attn: k and v must not be NULL");
+    if (!aligned16(d.k) || !aligned16(d.v)) CP_INVALID("cp_partial_attn: k and v must be 16-byte aligned");
+  }
+  if (d.in_dtype == CP_BF16 && d.skv > 0 && d.sq > 0) {
+    // tensor-map strides (row = heads * d * 2 bytes) must be multiples of 16 bytes
+    if ((int64_t(d.hq) * d.d * 2) % 16 != 0 || (int64_t(d.hkv) * d.d * 2) % 16 != 0)
+      CP_INVALID("cp_partial_attn: row strides must be multiples of 16 bytes");
+  }
+  if (d.sq == 0) return CP_OK;
+  int dev = 0, sms = 0;
+  cp_status st = require_sm103(&dev, &sms);
+  if (st != CP_OK) return st;
+  const float scale = d.scale > 0.0f ? d.scale : 1.0f / sqrtf(static_cast<float>(d.d));
+  const int64_t timeout_ns =
+      static_cast<int64_t>(d.wait_timeout_ms > 0 ? d.wait_timeout_ms : 2000) * 1000000LL;
+  if (d.in_dtype == CP_F32) return launch_partial_attn_simt(d, scale, timeout_ns, stream);
+  return launch_partial_attn_tc(d, scale, timeout_ns, sms, stream);
+}
+
+CP_API cp_status cp_merge_partials(int32_t n, const float* const* o_parts,
+                                   const float* const* lse_parts, int64_t sq, int32_t h, int32_t d,
+                                   void* o_out, int32_t out_dtype, float* lse_out,
+                                   cudaStream_t stream) {
+  clear_error();
+  if (n < 1 || n > CP_MAX_PARTIALS) CP_INVALID("cp_merge_partials: n=%d not in [1, %d]", n, CP_MAX_PARTIALS);
+  if (o_parts == nullptr || lse_parts == nullptr) CP_INVALID("cp_merge_partials: pointer arrays are NULL");
+  if (sq < 0) CP_INVALID("cp_merge_partials: negative row count");
+  if (h <= 0) CP_INVALID("cp_merge_partials: h must be positive");
+  if (d != 32 && d != 64 && d != 128 && d != 256) CP_INVALID("cp_merge_partials: d=%d not in {32, 64, 128, 256}", d);
+  if (out_dtype != CP_F32 && out_dtype != CP_BF16) CP_INVALID("cp_merge_partials: bad out_dtype %d", out_dtype);
+  if (sq == 0) return CP_OK;
+  if (o_out == nullptr || !aligned16(o_out)) CP_INVALID("cp_merge_partials: o_out NULL or not 16-byte aligned");
+  if (lse_out != nullptr && (reinterpret_cast<uintptr_t>(lse_out) & 3u)) CP_INVALID("cp_merge_partials: lse_out misaligned");
+  for (int i = 0; i < n; ++i) {
+    if (o_parts[i] == nullptr || lse_parts[i] == nullptr) CP_INVALID("cp_merge_partials: partial %d is NULL", i);
+    if (!aligned16(o_parts[i])) CP_INVALID("cp_merge_partials: partial %d O not 16-byte aligned", i);
+    if (reinterpret_cast<uintptr_t>(lse_parts[i]) & 3u) CP_INVALID("cp_merge_partials: partial %d LSE misaligned", i);
+  }
+  int sms = 0;
+  cp_status st = require_sm103(nullptr, &sms);
+  if (st != CP_OK) return st;
+  MergeArgs a{n, o_parts, lse_parts, sq, h, d, o_out, out_dtype == CP_BF16 ? 1 : 0, lse_out};
+  return launch_merge(a, sms, stream);
+}
+
+CP_API cp_status cp_ulysses_reshard(int32_t dir, int32_t cp, int64_t seq_len, int32_t n_tensors,
+                                    const int32_t* heads, int32_t d, int32_t dtype, int32_t layout,
+                                    const void* const* in, void* const* out, cudaStream_t stream) {
+  clear_error();
+  if (dir != 0 && dir != 1) CP_INVALID("cp_ulysses_reshard: dir must be 0 (seq->head) or 1 (head->seq)");
+  if (cp < 1) CP_INVALID("cp_ulysses_reshard: cp must be >= 1");
+  if (seq_len <= 0 || seq_len % cp != 0) CP_INVALID("cp_ulysses_reshard: seq_len %lld not a positive multiple of cp %d", (long long)seq_len, cp);
+  if (n_tensors < 1 || n_tensors > 4) CP_INVALID("cp_ulysses_reshard: n_tensors must be in [1, 4]");
+  if (heads == nullptr || in == nullptr || out == nullptr) CP_INVALID("cp_ulysses_reshard: NULL array argument");
+  if (d <= 0) CP_INVALID("cp_ulysses_reshard: d must be positive");
+  const int64_t es = dtype_size(dtype);
+  if (es == 0) CP_INVALID("cp_ulysses_reshard: bad dtype %d", dtype);
+  if (layout != CP_LAYOUT_CONTIGUOUS && layout != CP_LAYOUT_STRIDED) CP_INVALID("cp_ulysses_reshard: bad layout %d", layout);
+  if (cp > 64) CP_INVALID("cp_ulysses_reshard: cp must be <= 64");
+  for (int t = 0; t < n_tensors; ++t) {
+    if (heads[t] <= 0 || heads[t] % cp != 0) CP_INVALID("cp_ulysses_reshard: heads[%d]=%d not a positive multiple of cp %d", t, heads[t], cp);
+    if ((int64_t(heads[t] / cp) * d * es) % 16 != 0) CP_INVALID("cp_ulysses_reshard: per-rank head block of tensor %d is not a multiple of 16 bytes", t);
+    for (int r = 0; r < cp; ++r) {
+      const void* pi = in[t * cp + r];
+      const void* po = out[t * cp + r];
+      if (pi == nullptr || po == nullptr) CP_INVALID("cp_ulysses_reshard: NULL buffer (tensor %d, rank %d)", t, r);
+      if (!aligned16(pi) || !aligned16(po)) CP_INVALID("cp_ulysses_reshard: buffer not 16-byte aligned (tensor %d, rank %d)", t, r);
+    }
+  }
+  int sms = 0;
+  cp_status st = require_sm103(nullptr, &sms);
+  if (st != CP_OK) return st;
+  ReshardArgs a{dir, cp, n_tensors, seq_len, heads, d, static_cast<int32_t>(es), layout, in, out};
+  return launch_reshard(a, sms, stream);
+}

@@ -1,0 +1,55 @@
+// Internal declarations shared by the library's translation units (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "cpattn.h"
+
+#define CP_API extern "C" __attribute__((visibility("default")))
+
+namespace cpattn {
+
+// Records a printf-style message for cp_last_error() on the calling thread.
+void set_error(const char* fmt, ...);
+void clear_error();
+
+// Checks that the current device is an sm_103 part; caches per device.
+cp_status require_sm103(int* device_out, int* num_sms_out);
+
+// Maps a CUDA error to CP_ERR_CUDA with a message naming `what`.
+cp_status cuda_fail(cudaError_t e, const char* what);
+
+// ---- launchers (arguments already validated by the C entry points) ----
+cp_status launch_fill_positions(int32_t* out, int64_t n, int64_t base, int64_t stride,
+                                cudaStream_t s);
+
+cp_status launch_partial_attn_simt(const cp_attn_desc& d, float scale, int64_t timeout_ns,
+                                   cudaStream_t s);
+cp_status launch_partial_attn_tc(const cp_attn_desc& d, float scale, int64_t timeout_ns,
+                                 int num_sms, cudaStream_t s);
+
+struct MergeArgs {
+  int32_t n;
+  const float* const* o_parts;
+  const float* const* lse_parts;
+  int64_t sq;
+  int32_t h, d;
+  void* o_out;
+  int32_t out_bf16;
+  float* lse_out;
+};
+cp_status launch_merge(const MergeArgs& a, int num_sms, cudaStream_t s);
+
+struct ReshardArgs {
+  int32_t dir, cp, n_tensors;
+  int64_t seq_len;
+  const int32_t* heads;
+  int32_t d, esize;
+  int32_t layout;
+  const void* const* in;
+  void* const* out;
+};
+cp_status launch_reshard(const ReshardArgs& a, int num_sms, cudaStream_t s);
+
+}  // namespace cpattn

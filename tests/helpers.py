@@ -1,0 +1,55 @@
+"""Shared test helpers: build-once fixture logic and comparison utilities."""
+
+import os
+import re
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "cpattn.h")
+
+# Tolerances for floating point parity (max-abs), from the stated acceptance bars.
+TOL_F32 = 1e-5
+TOL_BF16_O = 2e-2
+TOL_BF16_LSE = 1e-3
+
+
+def ensure_built():
+    from context_blockwise_attention_gb300 import build as b
+    if not os.path.exists(b.LIB):
+        b.build()
+    return b.LIB
+
+
+def header_functions():
+    """Names of the functions declared in include/cpattn.h."""
+    with open(HEADER) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(cp_[a-z_0-9]+)\s*\(", src)))
+
+
+def max_abs(a, b, mask=None):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    if mask is not None:
+        a = a[mask]
+        b = b[mask]
+    if a.size == 0:
+        return 0.0
+    return float(np.abs(a - b).max())
+
+
+def compare_partial(o_gpu, l_gpu, o_ref, l_ref, tol_o, tol_l, what=""):
+    """O and LSE parity; rows with no visible key must be exactly O=0, LSE=-inf."""
+    o_gpu = np.asarray(o_gpu, dtype=np.float64)
+    l_gpu = np.asarray(l_gpu, dtype=np.float64)
+    empty = np.isneginf(l_ref)
+    assert np.array_equal(np.isneginf(l_gpu), empty), f"{what}: empty-row pattern differs"
+    assert np.all(o_gpu[empty] == 0.0), f"{what}: empty rows must have O = 0"
+    assert np.all(np.isfinite(o_gpu)), f"{what}: non-finite O"
+    eo = max_abs(o_gpu, o_ref)
+    el = max_abs(l_gpu, l_ref, ~empty)
+    assert eo <= tol_o, f"{what}: max|dO| = {eo:.3e} > {tol_o}"
+    assert el <= tol_l, f"{what}: max|dLSE| = {el:.3e} > {tol_l}"
+    return eo, el

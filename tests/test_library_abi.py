@@ -1,0 +1,133 @@
+"""The C ABI library: it loads, exports every function include/cpattn.h declares, and rejects
+invalid arguments on the host (no GPU work is issued by any of these calls)."""
+
+import ctypes
+
+import pytest
+
+import helpers
+
+helpers.ensure_built()
+
+import context_blockwise_attention_gb300 as cpa  # noqa: E402
+from context_blockwise_attention_gb300 import api  # noqa: E402
+
+
+def test_exports_every_declared_function():
+    declared = helpers.header_functions()
+    assert {"cp_shard_layout", "cp_partial_attn", "cp_merge_partials", "cp_ulysses_reshard",
+            "cp_last_error", "cp_version"} <= set(declared)
+    raw = ctypes.CDLL(cpa.library_path())
+    for name in declared:
+        assert hasattr(raw, name), f"{name} declared in cpattn.h but not exported"
+
+
+def test_version():
+    assert cpa.version() == 1
+
+
+def test_desc_layout_matches_header():
+    # the ctypes mirror must match the C struct size (pointers 8, int64 8, int32/float 4)
+    assert ctypes.sizeof(api._AttnDesc) == 136
+    assert ctypes.sizeof(api._PosMap) == 16
+
+
+def _layout(seq, cp, rank, kind):
+    lib = cpa.load_library()
+    m = api._PosMap()
+    st = lib.cp_shard_layout(seq, cp, rank, kind, ctypes.byref(m), None, None)
+    return st, m
+
+
+@pytest.mark.parametrize("seq,cp,rank,kind", [
+    (100, 8, 0, 0),   # not divisible
+    (64, 0, 0, 0),    # cp 0
+    (64, 4, 4, 0),    # rank out of range
+    (64, 4, -1, 1),
+    (-8, 4, 0, 0),
+    (64, 4, 0, 7),    # unknown kind
+])
+def test_layout_rejects(seq, cp, rank, kind):
+    st, _ = _layout(seq, cp, rank, kind)
+    assert st == api.CP_ERR_INVALID_ARG
+    assert cpa.load_library().cp_last_error()
+
+
+def test_layout_host_map_page_examples():
+    # host-only part (no positions buffer): the affine map
+    st, m = _layout(32768, 4, 1, api.CP_LAYOUT_CONTIGUOUS)
+    assert st == 0 and (m.base, m.stride) == (8192, 1)
+    st, m = _layout(64, 4, 1, api.CP_LAYOUT_STRIDED)
+    assert st == 0 and (m.base, m.stride) == (1, 4)
+
+
+def _desc(**kw):
+    d = api._AttnDesc()
+    d.q = d.k = d.v = 0x1000
+    d.o = 0x2000
+    d.lse = 0x3000
+    d.in_dtype = api.CP_BF16
+    d.o_dtype = api.CP_F32
+    d.sq, d.skv, d.hq, d.hkv, d.d = 128, 128, 8, 2, 128
+    d.causal = 1
+    d.q_pos = api._PosMap(0, 1)
+    d.kv_pos = api._PosMap(0, 1)
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+@pytest.mark.parametrize("field,value", [
+    ("d", 96), ("hq", 5), ("hkv", 0), ("in_dtype", 5), ("o_dtype", 9), ("causal", 2),
+    ("q", 0), ("k", 0), ("o", 0), ("lse", 0), ("q", 0x1008), ("sq", -1), ("flags", 0x40),
+    ("q_pos", api._PosMap(0, 0)), ("kv_pos", api._PosMap(-5, 1)), ("scale", -1.0),
+    ("wait_timeout_ms", -3),
+])
+def test_partial_attn_rejects(field, value):
+    lib = cpa.load_library()
+    d = _desc(**{field: value})
+    assert lib.cp_partial_attn(ctypes.byref(d), None) == api.CP_ERR_INVALID_ARG
+    assert lib.cp_last_error()
+
+
+def test_partial_attn_null_desc():
+    assert cpa.load_library().cp_partial_attn(None, None) == api.CP_ERR_INVALID_ARG
+
+
+def test_merge_rejects():
+    lib = cpa.load_library()
+    arr = (ctypes.c_void_p * 2)(0x1000, 0x2000)
+    out = ctypes.c_void_p(0x4000)
+    assert lib.cp_merge_partials(0, arr, arr, 8, 2, 64, out, 0, None, None) == api.CP_ERR_INVALID_ARG
+    assert lib.cp_merge_partials(129, arr, arr, 8, 2, 64, out, 0, None, None) == api.CP_ERR_INVALID_ARG
+    assert lib.cp_merge_partials(2, arr, arr, 8, 2, 48, out, 0, None, None) == api.CP_ERR_INVALID_ARG
+    assert lib.cp_merge_partials(2, arr, arr, 8, 2, 64, out, 3, None, None) == api.CP_ERR_INVALID_ARG
+    bad = (ctypes.c_void_p * 2)(0x1000, 0)
+    assert lib.cp_merge_partials(2, bad, arr, 8, 2, 64, out, 0, None, None) == api.CP_ERR_INVALID_ARG
+
+
+def test_reshard_rejects():
+    lib = cpa.load_library()
+    ptrs = (ctypes.c_void_p * 4)(0x1000, 0x2000, 0x3000, 0x4000)
+    heads = (ctypes.c_int32 * 1)(8)
+    ok_args = dict(dir=0, cp=4, seq=64, nt=1, d=64, dtype=1, layout=0)
+
+    def call(**kw):
+        a = dict(ok_args, **kw)
+        return lib.cp_ulysses_reshard(a["dir"], a["cp"], a["seq"], a["nt"], heads, a["d"],
+                                      a["dtype"], a["layout"], ptrs, ptrs, None)
+    assert call(dir=2) == api.CP_ERR_INVALID_ARG
+    assert call(seq=66) == api.CP_ERR_INVALID_ARG
+    assert call(cp=3) == api.CP_ERR_INVALID_ARG        # 8 heads not divisible by 3 (and 66 % 3)
+    assert call(dtype=4) == api.CP_ERR_INVALID_ARG
+    assert call(layout=3) == api.CP_ERR_INVALID_ARG
+    assert call(nt=0) == api.CP_ERR_INVALID_ARG
+    heads[0] = 6  # not a multiple of cp=4
+    assert call() == api.CP_ERR_INVALID_ARG
+
+
+def test_python_wrapper_rejects_cpu_tensors():
+    import torch
+    q = torch.zeros(4, 2, 64)
+    with pytest.raises(cpa.CpError):
+        cpa.partial_attn(q, q, q, cpa.PosMap(0, 1), cpa.PosMap(0, 1))

@@ -1,0 +1,73 @@
+"""Seeded generators and the library-side FLOP accounting (CPU only)."""
+
+import numpy as np
+import torch
+
+import oracle
+from context_blockwise_attention_gb300 import PosMap, visible_pairs
+from context_blockwise_attention_gb300 import workloads as wl
+
+
+def test_generators_are_seeded():
+    w = wl.WORKLOADS[2]
+    a = wl.shard_tensor(w, "q", 7, tokens=64)
+    b = wl.shard_tensor(w, "q", 7, tokens=64)
+    c = wl.shard_tensor(w, "q", 6, tokens=64)
+    assert a.dtype == torch.bfloat16 and torch.equal(a, b) and not torch.equal(a, c)
+    assert np.array_equal(wl.arrival_order(8, 5), wl.arrival_order(8, 5))
+    assert sorted(wl.arrival_order(64, 3)) == list(range(64))
+
+
+def test_outlier_fraction():
+    w = wl.WORKLOADS[5]
+    k = wl.shard_tensor(w, "k", 0, tokens=4096).float()
+    frac = (k.abs() > 5.0).float().mean().item()
+    assert 0.003 < frac < 0.02  # ~1% scaled by 8 (|N(0,1)|*8 > 5 about half the time)
+
+
+def test_ring_order_is_a_rotation():
+    for cp in (2, 4, 8):
+        for r in range(cp):
+            o = wl.ring_order(cp, r)
+            assert o[0] == r and sorted(o) == list(range(cp))
+
+
+def _pos_map(seq, cp, r, kind):
+    p = oracle.shard_positions(seq, cp, r, kind)
+    return PosMap(int(p[0]), int(p[1] - p[0]) if len(p) > 1 else 1), p
+
+
+def test_visible_pairs_matches_oracle_count():
+    for seq, cp in ((4096, 8), (1000, 4)):
+        for kind in ("contiguous", "strided"):
+            tot = 0
+            for r in range(cp):
+                qm, qp = _pos_map(seq, cp, r, kind)
+                for c in range(cp):
+                    km, kp = _pos_map(seq, cp, c, kind)
+                    n = visible_pairs(qm, len(qp), km, len(kp))
+                    assert n == oracle.visible_pair_count(qp, kp, True)
+                    tot += n
+            assert tot == seq * (seq + 1) // 2
+
+
+def test_workload_flop_counts():
+    # causal-adjusted FLOPs = 4 * D * Hq * N_vis for the bench configurations
+    w2 = wl.WORKLOADS[2]
+    qm, qp = _pos_map(w2.seq_len, w2.cp, 7, "strided")
+    n2 = sum(visible_pairs(qm, len(qp), _pos_map(w2.seq_len, w2.cp, c, "strided")[0], w2.local_len)
+             for c in range(w2.cp))
+    assert n2 == 67_125_248
+    assert abs(4 * 128 * 32 * n2 / 1e12 - 1.0998) < 1e-3
+    w3 = wl.WORKLOADS[3]
+    assert w3.seq_len * (w3.seq_len + 1) // 2 == 2_147_516_416
+    w5 = wl.WORKLOADS[5]
+    qm, qp = _pos_map(w5.seq_len, w5.cp, 7, "strided")
+    n5 = sum(visible_pairs(qm, len(qp), _pos_map(w5.seq_len, w5.cp, c, "strided")[0], w5.local_len)
+             for c in range(w5.cp))
+    assert n5 == 4_295_098_368
+
+
+def test_sample_rows_contains_required():
+    rows = wl.sample_rows(1000, 50, 1, must=[0, 999, 127, 128])
+    assert {0, 999, 127, 128} <= set(rows.tolist()) and len(rows) == 50
