@@ -76,6 +76,7 @@ class Step:
         self.reshard_bytes = 0
         self.launches = 0
         self.attn_calls = []      # list of (kwargs) for partial_attn
+        self.call_meta = []       # (query rank, source rank, sub-chunk) of each call
         self.merges = []          # list of (o_parts, l_parts, o_out, l_out)
         self.host_inputs = []     # (host pinned, device) pairs copied in e2e mode
         self.host_outputs = []    # (device, host pinned) pairs read back in e2e mode
@@ -100,11 +101,12 @@ class Step:
         self._input_tensors = []
         self._output_tensors = []
         self.pos_bufs = []
-        for r in sorted({c for c in range(w.cp)}):
+        for r in range(w.cp):
             k = wl.shard_tensor(w, "k", r, device=dev)
             v = wl.shard_tensor(w, "v", r, device=dev)
             kv[r] = (k, v)
             self._input_tensors += [k, v]
+        self.kv = kv
         self.rank_plans = []
         for qr in ranks:
             qmap = cpa.shard_layout(w.seq_len, w.cp, qr, self.layout)
@@ -127,6 +129,7 @@ class Step:
                 l = torch.empty((w.local_len, w.hq), dtype=torch.float32, device=dev)
                 self.attn_calls.append(dict(q=q, k=ks, v=vs, q_pos=qmap, kv_pos=kmap,
                                             causal=w.causal, o=o, lse=l))
+                self.call_meta.append((qr, src, sub))
                 self.flops += 4 * w.d * w.hq * n_vis
                 o_parts.append(o)
                 l_parts.append(l)
@@ -291,16 +294,20 @@ class ClockSampler:
 
 
 def _profile_traffic(kernel_file, workload_key):
-    """dram bytes per launch of the dominant kernel from the committed ncu summary, or None if
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, or None when
     the kernel source changed since the counters were taken."""
-    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    path = os.path.join(ROOT, "profiles", "attn_tc_kernel_traffic.txt")
     try:
-        with open(path) as f:
-            rec = json.load(f).get(workload_key)
         with open(kernel_file, "rb") as f:
             h = hashlib.sha256(f.read()).hexdigest()[:16]
-        if rec and rec.get("kernel_sha256_16") == h:
-            return float(rec["dram_bytes_per_launch"])
+        with open(path) as f:
+            for line in f:
+                parts = line.split()
+                if not parts or parts[0].startswith("#") or parts[0] != "workload":
+                    continue
+                kv = dict(zip(parts[0::2], parts[1::2]))
+                if kv.get("workload") == workload_key and kv.get("kernel_sha256_16") == h:
+                    return float(kv["dram_bytes_read"]) + float(kv["dram_bytes_write"])
     except Exception:
         pass
     return None
@@ -461,8 +468,9 @@ def run_gpu(args):
     value = world * step.flops / (ms_per_step * 1e-3) / 1e12
 
     def seg(name):
+        # total device time of one kind of launch per step (a step may record several intervals)
         xs = [s.elapsed_time(e) for s, e in timers[name]]
-        return sum(xs) / len(xs) if xs else None
+        return sum(xs) / args.steps if xs else None
     attn_ms = seg("attn")
     merge_ms = seg("merge")
     reshard_ms = seg("reshard")

@@ -1,0 +1,160 @@
+"""GPU parity at the benchmark workloads' full sizes, in the launch sequence bench.py times.
+
+Workloads 1 and 2: every row and head of every partial and of the merged output.
+Workloads 3-5: a seeded sample of query rows per rank (always including row 0, the last row,
+the rows on both sides of the first 128-row tile boundaries and, for workload 5, the first
+visible row of every chunk and the row just before it), all heads; every partial on the same
+rows.  The Ulysses reshards of workload 4 are compared bit for bit in full.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import helpers
+import oracle
+from helpers import TOL_BF16_LSE, TOL_BF16_O, TOL_F32, compare_partial
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    helpers.ensure_built()
+
+import bench  # noqa: E402
+from context_blockwise_attention_gb300 import workloads as wl  # noqa: E402
+
+DEV = torch.device("cuda", 0) if torch.cuda.is_available() else None
+
+
+def _rows_for(w, n_rows, sample):
+    if sample is None:
+        return np.arange(w.local_len)
+    must = [0, w.local_len - 1, 127, 128, 255, 256, 383, 384]
+    if w.chunks_per_shard > 1:
+        for c in range(w.chunks_per_shard):
+            must += [c * w.chunk_len, c * w.chunk_len - 1]
+    return wl.sample_rows(w.local_len, sample, seed=n_rows, must=must)
+
+
+def _check_rank_workload(cfg, layout, sample, query_ranks=None):
+    w = wl.WORKLOADS[cfg]
+    tol_o, tol_l = (TOL_F32, TOL_F32) if w.dtype == "f32" else (TOL_BF16_O, TOL_BF16_LSE)
+    steps = []
+    for qr in (query_ranks or [None]):
+        step = bench.Step(cfg, DEV, query_rank=qr, layout=layout)
+        for kw in step.attn_calls:  # poison outputs so unwritten rows cannot pass
+            kw["o"].fill_(float("nan"))
+            kw["lse"].fill_(float("nan"))
+        step.run()
+        torch.cuda.synchronize()
+        steps.append(step)
+    kv_cpu = {r: (k.cpu(), v.cpu()) for r, (k, v) in steps[0].kv.items()}
+    worst = [0.0, 0.0]
+    for step in steps:
+        for (qr, qmap, q, order), (o_parts, l_parts, out, lse) in zip(step.rank_plans, step.merges):
+            qpos = oracle.shard_positions(w.seq_len, w.cp, qr, layout)
+            rows = _rows_for(w, w.local_len + qr, sample)
+            q_rows = q[torch.from_numpy(rows).to(DEV)].cpu()
+            calls = [(i, m) for i, m in enumerate(step.call_meta) if m[0] == qr]
+            all_k, all_v, all_pos = [], [], []
+            for src in range(w.cp):
+                spos = oracle.shard_positions(w.seq_len, w.cp, src, layout)
+                all_k.append(kv_cpu[src][0])
+                all_v.append(kv_cpu[src][1])
+                all_pos.append(spos)
+            # every partial on the sampled rows
+            for i, (_, src, sub) in calls:
+                kw = step.attn_calls[i]
+                kpos = oracle.sub_chunk_positions(
+                    oracle.shard_positions(w.seq_len, w.cp, src, layout), sub, w.chunk_len)
+                lo, hi = sub * w.chunk_len, (sub + 1) * w.chunk_len
+                o_ref, l_ref = oracle.attention(q_rows, kv_cpu[src][0][lo:hi], kv_cpu[src][1][lo:hi],
+                                                qpos[rows], kpos, causal=w.causal)
+                idx = torch.from_numpy(rows).to(DEV)
+                eo, el = compare_partial(kw["o"][idx].float().cpu().numpy(), kw["lse"][idx].cpu().numpy(),
+                                         o_ref, l_ref, tol_o, tol_l, f"cfg{cfg} rank{qr} chunk({src},{sub})")
+                worst = [max(worst[0], eo), max(worst[1], el)]
+            # merged output against unsharded attention over every key
+            o_ref, l_ref = oracle.attention(q_rows, torch.cat(all_k), torch.cat(all_v), qpos[rows],
+                                            np.concatenate(all_pos), causal=w.causal)
+            idx = torch.from_numpy(rows).to(DEV)
+            eo, el = compare_partial(out[idx].float().cpu().numpy(), lse[idx].cpu().numpy(), o_ref,
+                                     l_ref, tol_o, tol_l, f"cfg{cfg} rank{qr} merged")
+            worst = [max(worst[0], eo), max(worst[1], el)]
+    return worst
+
+
+def test_cfg1_fp32_all_ranks_full():
+    # fp32 non-causal MHA S=512 CP=4: all 4 ranks, 4 chunks each in seeded random order
+    worst = _check_rank_workload(1, "contiguous", None)
+    assert worst[0] <= TOL_F32
+
+
+def test_cfg2_rank7_full():
+    # every row and head: 8 partials and the merged output
+    _check_rank_workload(2, "strided", None)
+
+
+def test_cfg2_rank0_sampled():
+    _check_rank_workload(2, "strided", 256, query_ranks=[0])
+
+
+@pytest.mark.parametrize("layout", ["strided", "contiguous"])
+def test_cfg3_all_ranks_sampled(layout):
+    _check_rank_workload(3, layout, 128)
+
+
+def test_cfg5_rank7_sampled_outliers():
+    _check_rank_workload(5, "strided", 128)
+
+
+def test_cfg4_ulysses():
+    w = wl.WORKLOADS[4]
+    cp, S = w.cp, w.seq_len
+    step = bench.Step(4, DEV)
+    for t in step.yo + step.ylse + step.xo:
+        t.fill_(float("nan"))
+    step.run()
+    torch.cuda.synchronize()
+    pos = [oracle.shard_positions(S, cp, r, w.layout) for r in range(cp)]
+    i16 = torch.int16
+
+    def ints(ts):
+        return [t.cpu().view(i16).numpy() for t in ts]
+    # seq -> head reshards, bit for bit
+    for src, dst in ((step.qs, step.yq), (step.ks, step.yk), (step.vs, step.yv)):
+        ref = oracle.seq_to_head(ints(src), pos)
+        for r in range(cp):
+            assert np.array_equal(dst[r].cpu().view(i16).numpy(), ref[r])
+    # head -> seq reshard, bit for bit, on generated data in the step's own buffers
+    hl, kl = w.hq // cp, w.hkv // cp
+    gen = [wl.normal((S, hl, w.d), torch.bfloat16, 900 + r, device=DEV) for r in range(cp)]
+    for r in range(cp):
+        step.yo[r].copy_(gen[r])
+    import context_blockwise_attention_gb300 as cpa
+    cpa.ulysses_reshard("head_to_seq", [step.yo], cp, S, w.layout, out=[step.xo])
+    torch.cuda.synchronize()
+    back = oracle.head_to_seq(ints(gen), pos)
+    for s in range(cp):
+        assert np.array_equal(step.xo[s].cpu().view(i16).numpy(), back[s])
+    # the whole step again, then attention on sampled rows against the unsharded inputs:
+    # per head-rank output (head-sharded) and the final sequence-sharded output
+    for t in step.yo + step.ylse + step.xo:
+        t.fill_(float("nan"))
+    step.run()
+    torch.cuda.synchronize()
+    q_full = torch.cat([x.cpu() for x in step.qs])  # contiguous layout: global order
+    k_full = torch.cat([x.cpu() for x in step.ks])
+    v_full = torch.cat([x.cpu() for x in step.vs])
+    gpos = np.arange(S)
+    rows = wl.sample_rows(S, 96, seed=4, must=[0, 1, 127, 128, S - 1, S // 2])
+    idx = torch.from_numpy(rows).to(DEV)
+    local = S // cp
+    for r in range(cp):
+        o_ref, l_ref = oracle.attention(q_full[rows][:, r * hl:(r + 1) * hl], k_full[:, r * kl:(r + 1) * kl],
+                                        v_full[:, r * kl:(r + 1) * kl], rows, gpos, causal=True)
+        compare_partial(step.yo[r][idx].float().cpu().numpy(), step.ylse[r][idx].cpu().numpy(), o_ref,
+                        l_ref, TOL_BF16_O, TOL_BF16_LSE, f"cfg4 head-rank {r}")
+        final = np.stack([step.xo[t // local][t % local, r * hl:(r + 1) * hl].float().cpu().numpy()
+                          for t in rows])
+        assert helpers.max_abs(final, o_ref) <= TOL_BF16_O, f"cfg4 final output, heads of rank {r}"
