@@ -81,18 +81,24 @@ struct Layout {
   static constexpr int kOffK = 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
-  // barriers: q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2],
-  //           o_final[2], never, drain
-  static constexpr int kNumBars = 1 + 4 * kStages + 6 + 2;
+  // barriers: q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_half[2],
+  //           p_full[2], o_final[2], never, drain
+  static constexpr int kNumBars = 1 + 4 * kStages + 8 + 2;
   static constexpr int kOffCtl = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffCtl + 16;
   static constexpr int kSmemLaunch = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
+// Register split (setmaxnreg): the TMA/MMA warpgroup gives registers to the two softmax
+// warpgroups.  4 warps x 56 + 8 warps x 224 = 12 warps x 168, the launch's allocation.
+constexpr uint32_t kRegsControl = 88;
+constexpr uint32_t kRegsSoftmax = 208;
+static_assert(4 * kRegsControl + 8 * kRegsSoftmax == 12 * 168, "register split must match launch");
+
 struct Bars {
   uint32_t q_full;
   uint32_t k_full, k_empty, v_full, v_empty;  // stage 0; +8 per stage
-  uint32_t s_full, p_full, o_final;           // tile A; +8 for tile B
+  uint32_t s_full, p_half, p_full, o_final;   // tile A; +8 for tile B
   uint32_t never, drain;
 };
 
@@ -109,7 +115,7 @@ __device__ __forceinline__ void raise_abort(const Ctl& c, int site) {
 
 // Waits for phase `parity` of `bar`; gives up (returns false) when the kernel is aborting or
 // when the wait exceeds the time limit, in which case it starts the abort itself.
-__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Ctl& c, int site) {
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Ctl& c, int site) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer();
   for (uint32_t it = 1;; ++it) {
@@ -124,8 +130,14 @@ __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const C
   }
 }
 
+// Every lane of the warp waits; the outcome is the same for the whole warp.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const Ctl& c, int site) {
+  const bool ok = wait_bounded(bar, parity, c, site);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // Teardown wait: ignores the abort flag (the copy or MMA must really finish) but stays bounded.
-__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, int64_t timeout_ns) {
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, int64_t timeout_ns) {
   const uint64_t t0 = ptx::globaltimer();
   while (!ptx::mbar_try_wait(bar, parity)) {
     if (static_cast<int64_t>(ptx::globaltimer() - t0) > timeout_ns) return;
@@ -138,6 +150,26 @@ __device__ __forceinline__ int64_t visible_keys(const TcParams& p, int64_t row) 
   if (qp < p.k_base) return 0;
   const int64_t n = (qp - p.k_base) / p.k_stride + 1;
   return n < p.skv ? n : p.skv;
+}
+
+// exp2 of 32 scaled scores (x = s * sl2 - m) packed to 16 bf16 pairs; adds the fp32 values to
+// the two packed partial sums.
+__device__ __forceinline__ void exp_pack32(const uint32_t (&s)[32], uint64_t sl2x2, uint64_t negm2,
+                                           uint32_t (&pk)[16], uint64_t& sum_a, uint64_t& sum_b) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const uint64_t x2 = ptx::f2_fma(ptx::f2_pack(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])),
+                                    sl2x2, negm2);
+    float x0, x1;
+    ptx::f2_unpack(x2, x0, x1);
+    const float p0 = ptx::ex2(x0);
+    const float p1 = ptx::ex2(x1);
+    pk[e] = ptx::pack_bf16x2(p0, p1);
+    if (e & 1)
+      sum_b = ptx::f2_add(sum_b, ptx::f2_pack(p0, p1));
+    else
+      sum_a = ptx::f2_add(sum_a, ptx::f2_pack(p0, p1));
+  }
 }
 
 template <int D>
@@ -173,7 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   b.v_full = b.k_empty + 8 * L::kStages;
   b.v_empty = b.v_full + 8 * L::kStages;
   b.s_full = b.v_empty + 8 * L::kStages;
-  b.p_full = b.s_full + 16;
+  b.p_half = b.s_full + 16;
+  b.p_full = b.p_half + 16;
   b.o_final = b.p_full + 16;
   b.never = b.o_final + 16;
   b.drain = b.never + 8;
@@ -192,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       ptx::mbar_init(b.s_full + 8 * t, 1);
+      ptx::mbar_init(b.p_half + 8 * t, 4);
       ptx::mbar_init(b.p_full + 8 * t, 4);
       ptx::mbar_init(b.o_final + 8 * t, 1);
     }
@@ -212,9 +246,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sK = sbase + L::kOffK;
   const uint32_t sV = sbase + L::kOffV;
 
-  if (warp == 0) {
+  if (warp < 4) {
+    ptx::regs_dec<kRegsControl>();
+  if (warp == 0 && n_tiles > 0) {
     // ================================================================ TMA producer
-    if (lane == 0 && n_tiles > 0) {
+    const bool leader = ptx::elect_one();
+    if (leader) {
       ptx::tma_prefetch_desc(&tm_q);
       ptx::tma_prefetch_desc(&tm_k);
       ptx::tma_prefetch_desc(&tm_v);
@@ -223,107 +260,140 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < L::kChunks; ++c)
           ptx::tma_load_2d(sQ + x * L::kTileBytes + c * L::kChunkBytes, &tm_q, h * D + c * 64,
                            static_cast<int32_t>(row0 + x * kRows), b.q_full);
-      int issued_k = 0, issued_v = 0;
-      for (int j = 0; j < n_tiles; ++j) {
-        const int t = p.descending ? n_tiles - 1 - j : j;
-        const int st = j % L::kStages;
-        const uint32_t ph = (j / L::kStages) & 1;
-        if (!wait_bounded(b.k_empty + 8 * st, ph ^ 1, ctl, kSiteKEmpty)) break;
+    }
+    __syncwarp();
+    int issued_k = 0, issued_v = 0;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int t = p.descending ? n_tiles - 1 - j : j;
+      const int st = j % L::kStages;
+      const uint32_t ph = (j / L::kStages) & 1;
+      if (!wait_warp(b.k_empty + 8 * st, ph ^ 1, ctl, kSiteKEmpty)) break;
+      if (leader) {
         ptx::mbar_arrive_expect_tx(b.k_full + 8 * st, L::kTileBytes);
         for (int c = 0; c < L::kChunks; ++c)
           ptx::tma_load_2d(sK + st * L::kTileBytes + c * L::kChunkBytes, &tm_k, kvh * D + c * 64,
                            t * kKeys, b.k_full + 8 * st);
-        issued_k = j + 1;
-        if (!wait_bounded(b.v_empty + 8 * st, ph ^ 1, ctl, kSiteVEmpty)) break;
+      }
+      __syncwarp();
+      issued_k = j + 1;
+      if (!wait_warp(b.v_empty + 8 * st, ph ^ 1, ctl, kSiteVEmpty)) break;
+      if (leader) {
         ptx::mbar_arrive_expect_tx(b.v_full + 8 * st, L::kTileBytes);
         for (int c = 0; c < L::kChunks; ++c)
           ptx::tma_load_2d(sV + st * L::kTileBytes + c * L::kChunkBytes, &tm_v, kvh * D + c * 64,
                            t * kKeys, b.v_full + 8 * st);
-        issued_v = j + 1;
       }
-      if (*abort_flag) {
-        // copies in flight must land before the CTA's shared memory goes away
-        wait_drain(b.q_full, 0, p.timeout_ns);
-        for (int s = 0; s < L::kStages; ++s) {
-          const int last_k = ((issued_k - 1 - s) >= 0) ? issued_k - 1 - ((issued_k - 1 - s) % L::kStages) : -1;
-          if (last_k >= 0) wait_drain(b.k_full + 8 * s, (last_k / L::kStages) & 1, p.timeout_ns);
-          const int last_v = ((issued_v - 1 - s) >= 0) ? issued_v - 1 - ((issued_v - 1 - s) % L::kStages) : -1;
-          if (last_v >= 0) wait_drain(b.v_full + 8 * s, (last_v / L::kStages) & 1, p.timeout_ns);
-        }
+      __syncwarp();
+      issued_v = j + 1;
+    }
+    if (*abort_flag && leader) {
+      // copies in flight must land before the CTA's shared memory goes away
+      wait_drain(b.q_full, 0, p.timeout_ns);
+      for (int s = 0; s < L::kStages; ++s) {
+        const int last_k = ((issued_k - 1 - s) >= 0) ? issued_k - 1 - ((issued_k - 1 - s) % L::kStages) : -1;
+        if (last_k >= 0) wait_drain(b.k_full + 8 * s, (last_k / L::kStages) & 1, p.timeout_ns);
+        const int last_v = ((issued_v - 1 - s) >= 0) ? issued_v - 1 - ((issued_v - 1 - s) % L::kStages) : -1;
+        if (last_v >= 0) wait_drain(b.v_full + 8 * s, (last_v / L::kStages) & 1, p.timeout_ns);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ================================================================ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(kRows, kKeys, 0, 0);
-      constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kRows, D, 0, 1);
-      const uint32_t tS[2] = {tmem + 0u, tmem + 128u};
-      const uint32_t tO[2] = {tmem + 256u, tmem + 384u};
-      bool ok = true;
-      if (p.test_stall && blockIdx.x == 0) ok = wait_bounded(b.never, 0, ctl, kSiteTest);
-      if (ok && n_tiles > 0) ok = wait_bounded(b.q_full, 0, ctl, kSiteQ);
+    // The whole warp runs the loop and waits; one elected lane issues each tcgen05 instruction.
+    const bool leader = ptx::elect_one();
+    constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(kRows, kKeys, 0, 0);
+    constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kRows, D, 0, 1);
+    // descriptor bases (start address field counts 16-byte units)
+    const uint64_t dQ0 = ptx::smem_desc_sw128(sQ, 16, 1024);
+    const uint64_t dK0 = ptx::smem_desc_sw128(sK, 16, 1024);
+    const uint64_t dV0 = ptx::smem_desc_sw128(sV, L::kChunkBytes, 1024);
+    constexpr uint64_t kTileUnits = L::kTileBytes >> 4;
+    bool ok = true;
+    if (p.test_stall && blockIdx.x == 0) ok = wait_warp(b.never, 0, ctl, kSiteTest);
+    if (ok && n_tiles > 0) ok = wait_warp(b.q_full, 0, ctl, kSiteQ);
 
-      auto issue_qk = [&](int x, int st) {
-        const uint32_t qa = sQ + x * L::kTileBytes;
-        const uint32_t ka = sK + st * L::kTileBytes;
+    auto issue_qk = [&](int x, int st) {
+      const uint64_t qd = dQ0 + x * kTileUnits;
+      const uint64_t kd = dK0 + st * kTileUnits;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
-          ptx::mma_ss(tS[x], ptx::smem_desc_sw128(qa + off, 16, 1024),
-                      ptx::smem_desc_sw128(ka + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
-        }
-      };
-      auto issue_pv = [&](int x, int st, bool acc) {
-        const uint32_t va = sV + st * L::kTileBytes;
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = static_cast<uint64_t>(((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4);
+        ptx::mma_ss(tmem + x * 128u, qd + off, kd + off, kIdescQK, kk > 0 ? 1u : 0u);
+      }
+    };
+    auto issue_pv = [&](int x, int st, int half, bool acc) {
+      const uint64_t vd = dV0 + st * kTileUnits;
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {
-          ptx::mma_ts(tO[x], tS[x] + kk * 8, ptx::smem_desc_sw128(va + kk * 2048, L::kChunkBytes, 1024),
-                      kIdescPV, (acc || kk > 0) ? 1u : 0u);
-        }
-      };
+      for (int q = 0; q < 4; ++q) {
+        const int kk = half * 4 + q;
+        ptx::mma_ts(tmem + 256u + x * 128u, tmem + x * 128u + kk * 8, vd + static_cast<uint64_t>(kk * 128),
+                    kIdescPV, (acc || kk > 0) ? 1u : 0u);
+      }
+    };
+    // PV for Q tile x on stage st: first half as soon as P's first 64 keys are in tensor memory
+    auto pv_tile = [&](int x, int st, int jj) -> bool {
+      if (!wait_warp(b.p_half + 8 * x, jj & 1, ctl, kSitePFull)) return false;
+      ptx::tc_fence_after();
+      if (leader) issue_pv(x, st, 0, jj > 0);
+      __syncwarp();
+      if (!wait_warp(b.p_full + 8 * x, jj & 1, ctl, kSitePFull)) return false;
+      ptx::tc_fence_after();
+      if (leader) issue_pv(x, st, 1, true);
+      __syncwarp();
+      return true;
+    };
 
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int st = j % L::kStages;
-        const uint32_t ph = (j / L::kStages) & 1;
-        if (!(ok = wait_bounded(b.k_full + 8 * st, ph, ctl, kSiteKFull))) break;
-        ptx::tc_fence_after();
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      const int st = j % L::kStages;
+      const uint32_t ph = (j / L::kStages) & 1;
+      if (!(ok = wait_warp(b.k_full + 8 * st, ph, ctl, kSiteKFull))) break;
+      ptx::tc_fence_after();
+      if (leader) {
         issue_qk(0, st);
         ptx::mma_commit(b.s_full);
-        if (j > 0) {
-          const int pst = (j - 1) % L::kStages;
-          if (!(ok = wait_bounded(b.p_full + 8, (j - 1) & 1, ctl, kSitePFull))) break;
-          ptx::tc_fence_after();
-          issue_pv(1, pst, j - 1 > 0);
-          ptx::mma_commit(b.v_empty + 8 * pst);
-        }
+      }
+      __syncwarp();
+      if (j > 0) {
+        const int pst = (j - 1) % L::kStages;
+        if (!(ok = pv_tile(1, pst, j - 1))) break;
+        if (leader) ptx::mma_commit(b.v_empty + 8 * pst);
+        __syncwarp();
+      }
+      if (leader) {
         issue_qk(1, st);
         ptx::mma_commit(b.s_full + 8);
         ptx::mma_commit(b.k_empty + 8 * st);
-        if (!(ok = wait_bounded(b.v_full + 8 * st, ph, ctl, kSiteVFull))) break;
-        if (!(ok = wait_bounded(b.p_full, j & 1, ctl, kSitePFull))) break;
-        ptx::tc_fence_after();
-        issue_pv(0, st, j > 0);
-        if (j == n_tiles - 1) ptx::mma_commit(b.o_final);
       }
-      if (ok && n_tiles > 0) {
-        const int j = n_tiles - 1;
-        const int st = j % L::kStages;
-        if ((ok = wait_bounded(b.p_full + 8, j & 1, ctl, kSitePFull))) {
-          ptx::tc_fence_after();
-          issue_pv(1, st, j > 0);
+      __syncwarp();
+      if (!(ok = wait_warp(b.v_full + 8 * st, ph, ctl, kSiteVFull))) break;
+      if (!(ok = pv_tile(0, st, j))) break;
+      if (j == n_tiles - 1) {
+        if (leader) ptx::mma_commit(b.o_final);
+        __syncwarp();
+      }
+    }
+    if (ok && n_tiles > 0) {
+      const int j = n_tiles - 1;
+      const int st = j % L::kStages;
+      if ((ok = pv_tile(1, st, j))) {
+        if (leader) {
           ptx::mma_commit(b.v_empty + 8 * st);
           ptx::mma_commit(b.o_final + 8);
         }
+        __syncwarp();
       }
-      if (!ok) {
-        // every MMA issued so far must complete before tensor memory is released
+    }
+    if (!ok) {
+      // every MMA issued so far must complete before tensor memory is released
+      if (leader) {
         ptx::mma_commit(b.drain);
         wait_drain(b.drain, 0, p.timeout_ns);
       }
+      __syncwarp();
     }
-    __syncwarp();
-  } else if (warp >= 4) {
+  }
+  } else {
+    ptx::regs_inc<kRegsSoftmax>();
     // ================================================================ softmax warpgroups
     const int x = (warp - 4) >> 2;           // 0: tile A, 1: tile B
     const int wq = warp & 3;                 // lane quarter of tensor memory
@@ -336,6 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t lim = p.causal ? visible_keys(p, grow) : p.skv;
     const int64_t q_first = p.q_base + p.q_stride * tile_row0;
     const float sl2 = p.scale_log2;
+    const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
 
     float m_ref = -INFINITY;  // running maximum (log2 units of scaled scores)
     float l = 0.0f;           // running sum of 2^(x - m_ref)
@@ -343,11 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     for (int j = 0; j < n_tiles; ++j) {
       const int t = p.descending ? n_tiles - 1 - j : j;
-      ok = wait_bounded(b.s_full + 8 * x, j & 1, ctl, kSiteSFull);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
+      if (!(ok = wait_warp(b.s_full + 8 * x, j & 1, ctl, kSiteSFull))) break;
       ptx::tc_fence_after();
       uint32_t sr[4][32];
 #pragma unroll
@@ -357,23 +424,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t k0 = static_cast<int64_t>(t) * kKeys;
       const bool need_mask =
           (k0 + kKeys > p.skv) || (p.causal && p.k_base + p.k_stride * (k0 + kKeys - 1) > q_first);
-      float mx = -INFINITY;
       if (need_mask) {
         const int64_t lim_local = lim - k0;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float v = (c * 32 + e < lim_local) ? __uint_as_float(sr[c][e]) : -INFINITY;
-            sr[c][e] = __float_as_uint(v);
-            mx = fmaxf(mx, v);
-          }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[c][e]));
+          for (int e = 0; e < 32; ++e)
+            if (c * 32 + e >= lim_local) sr[c][e] = __float_as_uint(-INFINITY);
       }
+      // row maximum: four independent 3-input max chains
+      float a0 = fmaxf(__uint_as_float(sr[0][0]), __uint_as_float(sr[0][1]));
+      float a1 = fmaxf(__uint_as_float(sr[0][2]), __uint_as_float(sr[0][3]));
+      float a2 = fmaxf(__uint_as_float(sr[0][4]), __uint_as_float(sr[0][5]));
+      float a3 = fmaxf(__uint_as_float(sr[0][6]), __uint_as_float(sr[0][7]));
+#pragma unroll
+      for (int i = 8; i < 128; i += 8) {
+        a0 = ptx::max3(a0, __uint_as_float(sr[i >> 5][(i + 0) & 31]), __uint_as_float(sr[i >> 5][(i + 1) & 31]));
+        a1 = ptx::max3(a1, __uint_as_float(sr[i >> 5][(i + 2) & 31]), __uint_as_float(sr[i >> 5][(i + 3) & 31]));
+        a2 = ptx::max3(a2, __uint_as_float(sr[i >> 5][(i + 4) & 31]), __uint_as_float(sr[i >> 5][(i + 5) & 31]));
+        a3 = ptx::max3(a3, __uint_as_float(sr[i >> 5][(i + 6) & 31]), __uint_as_float(sr[i >> 5][(i + 7) & 31]));
+      }
+      const float mx = ptx::max3(a0, a1, fmaxf(a2, a3));
       const float m_tile = mx * sl2;  // -inf stays -inf
       bool rescale = false;
       float factor = 1.0f;
@@ -397,28 +468,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
+      const uint64_t negm2 = ptx::f2_pack(-m_use, -m_use);
+      uint64_t sum_a = ptx::f2_pack(0.0f, 0.0f), sum_b = sum_a;
+      // keys 0..63: P released early so the PV product can start on them
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t pk[16];
+        exp_pack32(sr[c], sl2x2, negm2, pk, sum_a, sum_b);
+        ptx::tmem_st16(tS + c * 16, pk);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(b.p_half + 8 * x);
+      // keys 64..127
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p0 = ptx::ex2(fmaf(__uint_as_float(sr[c][2 * e]), sl2, -m_use));
-          const float p1 = ptx::ex2(fmaf(__uint_as_float(sr[c][2 * e + 1]), sl2, -m_use));
-          l += p0 + p1;
-          pk[e] = ptx::pack_bf16x2(p0, p1);
-        }
+      for (int c = 2; c < 4; ++c) {
+        uint32_t pk[16];
+        exp_pack32(sr[c], sl2x2, negm2, pk, sum_a, sum_b);
         ptx::tmem_st16(tS + c * 16, pk);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(b.p_full + 8 * x);
+      float s0, s1, s2, s3;
+      ptx::f2_unpack(sum_a, s0, s1);
+      ptx::f2_unpack(sum_b, s2, s3);
+      l += (s0 + s1) + (s2 + s3);
     }
 
     // ---------------------------------------------------------------- epilogue
     if (ok && n_tiles > 0) {
-      ok = wait_bounded(b.o_final + 8 * x, 0, ctl, kSiteOFinal);
-      ok = __all_sync(0xffffffffu, ok);
+      ok = wait_warp(b.o_final + 8 * x, 0, ctl, kSiteOFinal);
       if (ok) ptx::tc_fence_after();
     }
     if (ok) {

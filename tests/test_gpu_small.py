@@ -227,7 +227,9 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     dt = time.time() - t0
     st = status.item()
     assert st & 0xff == api.CP_ERR_TIMEOUT, st
-    assert (st >> 8) == 9  # the test barrier's site
+    # the site of whichever bounded wait expired first: the injected one (9) or a wait that
+    # depends on it (the stalled MMA warp starves the S/P/O handshakes and the TMA ring)
+    assert (st >> 8) in range(1, 10), st
     assert dt < 10.0
     # the context is still usable and a normal call is correct
     o, l, o_ref, l_ref = _run_partial(sq, skv, hq, hkv, d, True, PosMap(0, 1), PosMap(0, 1),
