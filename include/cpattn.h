@@ -140,7 +140,7 @@ cp_status cp_partial_attn(const cp_attn_desc* desc, cudaStream_t stream);
  *   n          1 <= n <= CP_MAX_PARTIALS
  *   o_parts    host array of n device pointers, each fp32 [sq, h, d]
  *   lse_parts  host array of n device pointers, each fp32 [sq, h]
- *   sq, h, d   rows, heads, head_dim (d % 4 == 0, d <= 256)
+ *   sq, h, d   rows, heads, head_dim (d in {32, 64, 128, 256})
  *   o_out      device [sq, h, d] in out_dtype (CP_F32 or CP_BF16, round-to-nearest-even)
  *   lse_out    device fp32 [sq, h], or NULL to skip
  * Errors: CP_ERR_INVALID_ARG (n out of range, null or unaligned pointers, bad sizes),
@@ -159,7 +159,7 @@ cp_status cp_merge_partials(int32_t n, const float* const* o_parts, const float*
  *   where pos_s is shard s's layout (cp_shard_layout) and t indexes the tensors of one call.
  * Arguments:
  *   dir        0 or 1
- *   cp         number of ranks (>= 1); seq_len % cp == 0
+ *   cp         number of ranks, 1 <= cp <= 64; seq_len % cp == 0
  *   n_tensors  1..4 tensors moved in one launch (e.g. 2 for fused K|V)
  *   heads      host array [n_tensors]: full head count H_t of each tensor; H_t % cp == 0
  *   d          head_dim; (H_t/cp) * d * sizeof(dtype) must be a multiple of 16 bytes
