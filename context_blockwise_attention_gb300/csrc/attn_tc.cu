@@ -175,7 +175,8 @@ __device__ __forceinline__ void exp_pack32(const uint32_t (&s)[32], uint64_t sl2
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tm_q,
-                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                   const __grid_constant__ CUtensorMap tm_o) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -499,15 +500,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---------------------------------------------------------------- epilogue
-    if (ok && n_tiles > 0) {
-      ok = wait_warp(b.o_final + 8 * x, 0, ctl, kSiteOFinal);
-      if (ok) ptx::tc_fence_after();
-    }
+    if (ok && n_tiles > 0) ok = wait_warp(b.o_final + 8 * x, 0, ctl, kSiteOFinal);
+    // every warp of the warpgroup arrives here exactly once; the epilogue's own barrier below
+    // is entered only if all four warps finished their loop and saw the final O
+    ok = ptx::named_bar_and(1 + x, 128, ok);
     if (ok) {
+      if (n_tiles > 0) ptx::tc_fence_after();
+      // O / l staged in shared memory in the 128-byte-swizzled box layout of the output map,
+      // then written by TMA (whole 128-byte lines; rows past sq are clipped by the map).  Tile A
+      // stages in the K ring, tile B in the V ring: once o_final of a tile has fired, every QK
+      // (for A) or every MMA (for B) has completed, so those rings are idle.
       const bool has = (m_ref != -INFINITY) && (l > 0.0f);
       const float inv = has ? 1.0f / l : 0.0f;
-      const bool row_ok = grow < p.sq;
-      const int64_t obase = (grow * p.hq + h) * static_cast<int64_t>(D);
+      const uint32_t stage = x == 0 ? sK : sV;
+      const uint32_t row_base = stage + static_cast<uint32_t>(r) * 128u;
+      const uint32_t sw = static_cast<uint32_t>(r & 7);
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -518,29 +525,44 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = 0u;
         }
-        if (row_ok) {
-          if (p.o_bf16) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + obase + c * 32);
+        if (p.o_bf16) {
+          // box = 64 bf16 columns; columns [32c, 32c+32) are 16-byte chunks 4(c&1) .. 4(c&1)+3
+          const uint32_t box = stage + static_cast<uint32_t>(c >> 1) * 16384u;
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              uint4 w;
-              w.x = ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 0]) * inv, __uint_as_float(o[8 * q4 + 1]) * inv);
-              w.y = ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv, __uint_as_float(o[8 * q4 + 3]) * inv);
-              w.z = ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv, __uint_as_float(o[8 * q4 + 5]) * inv);
-              w.w = ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv, __uint_as_float(o[8 * q4 + 7]) * inv);
-              dst[q4] = w;
-            }
-          } else {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + obase + c * 32);
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const uint32_t chunk = static_cast<uint32_t>((c & 1) * 4 + q4);
+            const uint32_t a = box + static_cast<uint32_t>(r) * 128u + ((chunk ^ sw) << 4);
+            const uint32_t w0 = ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 0]) * inv, __uint_as_float(o[8 * q4 + 1]) * inv);
+            const uint32_t w1 = ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv, __uint_as_float(o[8 * q4 + 3]) * inv);
+            const uint32_t w2 = ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv, __uint_as_float(o[8 * q4 + 5]) * inv);
+            const uint32_t w3 = ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv, __uint_as_float(o[8 * q4 + 7]) * inv);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w0), "r"(w1), "r"(w2), "r"(w3) : "memory");
+          }
+        } else {
+          // box = 32 fp32 columns = 8 chunks of 16 bytes
+          const uint32_t box = row_base + static_cast<uint32_t>(c) * 16384u;
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4)
-              dst[q4] = make_float4(__uint_as_float(o[4 * q4 + 0]) * inv, __uint_as_float(o[4 * q4 + 1]) * inv,
-                                    __uint_as_float(o[4 * q4 + 2]) * inv, __uint_as_float(o[4 * q4 + 3]) * inv);
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const uint32_t a = box + ((static_cast<uint32_t>(q4) ^ sw) << 4);
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                         "f"(__uint_as_float(o[4 * q4 + 0]) * inv), "f"(__uint_as_float(o[4 * q4 + 1]) * inv),
+                         "f"(__uint_as_float(o[4 * q4 + 2]) * inv), "f"(__uint_as_float(o[4 * q4 + 3]) * inv)
+                         : "memory");
           }
         }
       }
-      if (row_ok)
+      ptx::fence_proxy_async_smem();
+      ptx::named_bar_sync(1 + x, 128);
+      if (wq == 0 && lane == 0) {
+        const int boxes = p.o_bf16 ? (D / 64) : (D / 32);
+        const int box_cols = p.o_bf16 ? 64 : 32;
+        for (int c = 0; c < boxes; ++c)
+          ptx::tma_store_2d(&tm_o, stage + c * 16384u, h * D + c * box_cols, static_cast<int32_t>(tile_row0));
+        ptx::bulk_commit();
+      }
+      if (grow < p.sq)
         p.lse[grow * p.hq + h] = has ? (m_ref * 0.69314718055994531f + logf(l)) : -INFINITY;
+      if (wq == 0 && lane == 0) ptx::bulk_wait_all();
     }
   }
 
@@ -584,28 +606,31 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// 2-D map over a token-major bf16 tensor viewed as [tokens, heads*d]; box = 64 columns x 128 rows
-// with 128-byte swizzle (the canonical K-major / MN-major UMMA layout).
-bool make_map(CUtensorMap* m, const void* base, int64_t tokens, int64_t row_elems) {
+// 2-D map over a token-major tensor viewed as [tokens, heads*d]; box = 128 bytes of columns x
+// 128 rows with 128-byte swizzle (for bf16 operands: the canonical K-major / MN-major UMMA
+// layout; for the output: the staging layout of the epilogue).
+bool make_map(CUtensorMap* m, const void* base, int64_t tokens, int64_t row_elems, bool fp32 = false) {
   EncodeTiledFn enc = get_encode_fn();
   if (enc == nullptr) return false;
+  const int64_t es = fp32 ? 4 : 2;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_elems), static_cast<cuuint64_t>(tokens)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_elems * 2)};
-  cuuint32_t box[2] = {64, 128};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_elems * es)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / es), 128};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
 template <int D>
 cp_status launch_tc(const TcParams& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                    int64_t grid, cudaStream_t s) {
+                    const CUtensorMap& mo, int64_t grid, cudaStream_t s) {
   constexpr int smem = Layout<D>::kSmemLaunch;
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attn_tc_kernel)");
-  attn_tc_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p, mq, mk, mv);
+  attn_tc_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p, mq, mk, mv, mo);
   e = cudaGetLastError();
   return e == cudaSuccess ? CP_OK : cuda_fail(e, "attn_tc_kernel launch");
 }
@@ -643,9 +668,10 @@ cp_status launch_partial_attn_tc(const cp_attn_desc& d, float scale, int64_t tim
   p.k_base = d.kv_pos.base;
   p.k_stride = d.kv_pos.stride;
   p.timeout_ns = timeout_ns;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!make_map(&mq, d.q, d.sq, int64_t(d.hq) * d.d) || !make_map(&mk, d.k, d.skv, int64_t(d.hkv) * d.d) ||
-      !make_map(&mv, d.v, d.skv, int64_t(d.hkv) * d.d)) {
+      !make_map(&mv, d.v, d.skv, int64_t(d.hkv) * d.d) ||
+      !make_map(&mo, d.o, d.sq, int64_t(d.hq) * d.d, d.o_dtype == CP_F32)) {
     set_error("cuTensorMapEncodeTiled failed (or the driver entry point is unavailable)");
     return CP_ERR_CUDA;
   }
@@ -654,8 +680,8 @@ cp_status launch_partial_attn_tc(const cp_attn_desc& d, float scale, int64_t tim
     set_error("partial attention grid too large");
     return CP_ERR_INVALID_ARG;
   }
-  if (d.d == 64) return launch_tc<64>(p, mq, mk, mv, grid, s);
-  return launch_tc<128>(p, mq, mk, mv, grid, s);
+  if (d.d == 64) return launch_tc<64>(p, mq, mk, mv, mo, grid, s);
+  return launch_tc<128>(p, mq, mk, mv, mo, grid, s);
 }
 
 }  // namespace cpattn
