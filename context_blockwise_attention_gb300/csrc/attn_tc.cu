@@ -56,6 +56,8 @@ enum WaitSite : int {
   kSitePFull = 7,
   kSiteOFinal = 8,
   kSiteTest = 9,
+  kSiteSFree = 10,
+  kSitePvDone = 11,
 };
 
 struct TcParams {
@@ -82,8 +84,15 @@ struct Layout {
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
   // barriers: q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_half[2],
-  //           p_full[2], o_final[2], never, drain
-  static constexpr int kNumBars = 1 + 4 * kStages + 8 + 2;
+  //           p_full[2], o_final[2], s_free[2], pv_done[2], never, drain
+  static constexpr int kNumBars = 1 + 4 * kStages + 12 + 2;
+  // Tensor memory: S_A, S_B at columns 0 / 128.  D=128: O_A, O_B at 256 / 384 and P written over
+  // the first 64 columns of its S tile.  D=64: O_A, O_B at 256 / 320 and separate P_A, P_B at
+  // 384 / 448, so a tile's S can be overwritten by the next QK while its P still feeds the PV
+  // product ("decoupled P").
+  static constexpr bool kSepP = (D == 64);
+  static constexpr uint32_t kColO = 256, kStrideO = kSepP ? 64 : 128;
+  static constexpr uint32_t kColP = kSepP ? 384 : 0, kStrideP = kSepP ? 64 : 128;
   static constexpr int kOffCtl = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffCtl + 16;
   static constexpr int kSmemLaunch = kBytes + 1024;  // slack for 1024-byte alignment
@@ -99,6 +108,7 @@ struct Bars {
   uint32_t q_full;
   uint32_t k_full, k_empty, v_full, v_empty;  // stage 0; +8 per stage
   uint32_t s_full, p_half, p_full, o_final;   // tile A; +8 for tile B
+  uint32_t s_free, pv_done;                   // tile A; +8 for tile B (decoupled P only)
   uint32_t never, drain;
 };
 
@@ -116,7 +126,9 @@ __device__ __forceinline__ void raise_abort(const Ctl& c, int site) {
 // Waits for phase `parity` of `bar`; gives up (returns false) when the kernel is aborting or
 // when the wait exceeds the time limit, in which case it starts the abort itself.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Ctl& c, int site) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
+  // a phase that has already completed is seen by the non-blocking test at once; try_wait may
+  // suspend the thread for a time slice even then
+  if (ptx::mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
@@ -153,7 +165,9 @@ __device__ __forceinline__ int64_t visible_keys(const TcParams& p, int64_t row) 
 }
 
 // exp2 of 32 scaled scores (x = s * sl2 - m) packed to 16 bf16 pairs; adds the fp32 values to
-// the two packed partial sums.
+// the two packed partial sums.  (Evaluating part of the exponentials with a polynomial on the FMA
+// pipe was measured slower on GB300 for both head dims: the softmax is bound by instruction issue
+// and latency, not by the MUFU unit.)
 __device__ __forceinline__ void exp_pack32(const uint32_t (&s)[32], uint64_t sl2x2, uint64_t negm2,
                                            uint32_t (&pk)[16], uint64_t& sum_a, uint64_t& sum_b) {
 #pragma unroll
@@ -209,7 +223,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   b.p_half = b.s_full + 16;
   b.p_full = b.p_half + 16;
   b.o_final = b.p_full + 16;
-  b.never = b.o_final + 16;
+  b.s_free = b.o_final + 16;
+  b.pv_done = b.s_free + 16;
+  b.never = b.pv_done + 16;
   b.drain = b.never + 8;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffCtl);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffCtl + 4);
@@ -229,6 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(b.p_half + 8 * t, 4);
       ptx::mbar_init(b.p_full + 8 * t, 4);
       ptx::mbar_init(b.o_final + 8 * t, 1);
+      ptx::mbar_init(b.s_free + 8 * t, 4);
+      ptx::mbar_init(b.pv_done + 8 * t, 1);
     }
     ptx::mbar_init(b.never, 1);
     ptx::mbar_init(b.drain, 1);
@@ -327,8 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int kk = half * 4 + q;
-        ptx::mma_ts(tmem + 256u + x * 128u, tmem + x * 128u + kk * 8, vd + static_cast<uint64_t>(kk * 128),
-                    kIdescPV, (acc || kk > 0) ? 1u : 0u);
+        ptx::mma_ts(tmem + L::kColO + x * L::kStrideO, tmem + L::kColP + x * L::kStrideP + kk * 8,
+                    vd + static_cast<uint64_t>(kk * 128), kIdescPV, (acc || kk > 0) ? 1u : 0u);
       }
     };
     // PV for Q tile x on stage st: first half as soon as P's first 64 keys are in tensor memory
@@ -344,44 +362,103 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
 
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      const int st = j % L::kStages;
-      const uint32_t ph = (j / L::kStages) & 1;
-      if (!(ok = wait_warp(b.k_full + 8 * st, ph, ctl, kSiteKFull))) break;
-      ptx::tc_fence_after();
-      if (leader) {
-        issue_qk(0, st);
-        ptx::mma_commit(b.s_full);
-      }
-      __syncwarp();
-      if (j > 0) {
-        const int pst = (j - 1) % L::kStages;
-        if (!(ok = pv_tile(1, pst, j - 1))) break;
-        if (leader) ptx::mma_commit(b.v_empty + 8 * pst);
-        __syncwarp();
-      }
-      if (leader) {
-        issue_qk(1, st);
-        ptx::mma_commit(b.s_full + 8);
-        ptx::mma_commit(b.k_empty + 8 * st);
-      }
-      __syncwarp();
-      if (!(ok = wait_warp(b.v_full + 8 * st, ph, ctl, kSiteVFull))) break;
-      if (!(ok = pv_tile(0, st, j))) break;
-      if (j == n_tiles - 1) {
-        if (leader) ptx::mma_commit(b.o_final);
-        __syncwarp();
-      }
-    }
-    if (ok && n_tiles > 0) {
-      const int j = n_tiles - 1;
-      const int st = j % L::kStages;
-      if ((ok = pv_tile(1, st, j))) {
+    if constexpr (L::kSepP) {
+      // QK_A(j), QK_B(j) as soon as the softmax warpgroups have copied S(j-1) to registers; the
+      // PV products of step j-1 follow, each gated by its P.
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int st = j % L::kStages;
+        const uint32_t ph = (j / L::kStages) & 1;
+        if (!(ok = wait_warp(b.k_full + 8 * st, ph, ctl, kSiteKFull))) break;
+        if (j > 0 && !(ok = wait_warp(b.s_free, (j - 1) & 1, ctl, kSiteSFree))) break;
+        ptx::tc_fence_after();
         if (leader) {
-          ptx::mma_commit(b.v_empty + 8 * st);
-          ptx::mma_commit(b.o_final + 8);
+          issue_qk(0, st);
+          ptx::mma_commit(b.s_full);
         }
         __syncwarp();
+        if (j > 0 && !(ok = wait_warp(b.s_free + 8, (j - 1) & 1, ctl, kSiteSFree))) break;
+        ptx::tc_fence_after();
+        if (leader) {
+          issue_qk(1, st);
+          ptx::mma_commit(b.s_full + 8);
+          ptx::mma_commit(b.k_empty + 8 * st);
+        }
+        __syncwarp();
+        if (j > 0) {
+          const int pj = j - 1;
+          const int pst = pj % L::kStages;
+          if (!(ok = wait_warp(b.v_full + 8 * pst, (pj / L::kStages) & 1, ctl, kSiteVFull))) break;
+          if (!(ok = pv_tile(0, pst, pj))) break;
+          if (leader) ptx::mma_commit(b.pv_done);
+          __syncwarp();
+          if (!(ok = pv_tile(1, pst, pj))) break;
+          if (leader) {
+            ptx::mma_commit(b.pv_done + 8);
+            ptx::mma_commit(b.v_empty + 8 * pst);
+          }
+          __syncwarp();
+        }
+      }
+      if (ok && n_tiles > 0) {
+        const int pj = n_tiles - 1;
+        const int pst = pj % L::kStages;
+        ok = wait_warp(b.v_full + 8 * pst, (pj / L::kStages) & 1, ctl, kSiteVFull);
+        if (ok && (ok = pv_tile(0, pst, pj))) {
+          if (leader) {
+            ptx::mma_commit(b.pv_done);
+            ptx::mma_commit(b.o_final);
+          }
+          __syncwarp();
+          if ((ok = pv_tile(1, pst, pj))) {
+            if (leader) {
+              ptx::mma_commit(b.pv_done + 8);
+              ptx::mma_commit(b.v_empty + 8 * pst);
+              ptx::mma_commit(b.o_final + 8);
+            }
+            __syncwarp();
+          }
+        }
+      }
+    } else {
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int st = j % L::kStages;
+        const uint32_t ph = (j / L::kStages) & 1;
+        if (!(ok = wait_warp(b.k_full + 8 * st, ph, ctl, kSiteKFull))) break;
+        ptx::tc_fence_after();
+        if (leader) {
+          issue_qk(0, st);
+          ptx::mma_commit(b.s_full);
+        }
+        __syncwarp();
+        if (j > 0) {
+          const int pst = (j - 1) % L::kStages;
+          if (!(ok = pv_tile(1, pst, j - 1))) break;
+          if (leader) ptx::mma_commit(b.v_empty + 8 * pst);
+          __syncwarp();
+        }
+        if (leader) {
+          issue_qk(1, st);
+          ptx::mma_commit(b.s_full + 8);
+          ptx::mma_commit(b.k_empty + 8 * st);
+        }
+        __syncwarp();
+        if (!(ok = wait_warp(b.v_full + 8 * st, ph, ctl, kSiteVFull))) break;
+        if (!(ok = pv_tile(0, st, j))) break;
+        if (j == n_tiles - 1) {
+          if (leader) ptx::mma_commit(b.o_final);
+          __syncwarp();
+        }
+      }
+      if (ok && n_tiles > 0) {
+        const int j = n_tiles - 1;
+        const int st = j % L::kStages;
+        if ((ok = pv_tile(1, st, j))) {
+          if (leader) {
+            ptx::mma_commit(b.v_empty + 8 * st);
+            ptx::mma_commit(b.o_final + 8);
+          }
+          __syncwarp();
+        }
       }
     }
     if (!ok) {
@@ -401,7 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = wq * 32 + lane;            // row inside the tile
     const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + x * 128u + lane_bits;
-    const uint32_t tO = tmem + 256u + x * 128u + lane_bits;
+    const uint32_t tO = tmem + L::kColO + x * L::kStrideO + lane_bits;
+    const uint32_t tP = tmem + L::kColP + x * L::kStrideP + lane_bits;
     const int64_t tile_row0 = row0 + x * kRows;
     const int64_t grow = tile_row0 + r;
     const int64_t lim = p.causal ? visible_keys(p, grow) : p.skv;
@@ -421,6 +499,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + c * 32, sr[c]);
       ptx::tmem_wait_ld();
+      // decoupled P: S is in registers, the next QK may overwrite it
+      bool pv_seen = true;
+      if constexpr (L::kSepP) {
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(b.s_free + 8 * x);
+        pv_seen = (j == 0);
+      }
+      // decoupled P: O and P_x may only be touched once PV_x(j-1) has completed
+      auto wait_pv = [&]() -> bool {
+        if (pv_seen) return true;
+        pv_seen = true;
+        if (!wait_warp(b.pv_done + 8 * x, (j - 1) & 1, ctl, kSitePvDone)) return false;
+        ptx::tc_fence_after();
+        return true;
+      };
 
       const int64_t k0 = static_cast<int64_t>(t) * kKeys;
       const bool need_mask =
@@ -433,19 +527,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 32; ++e)
             if (c * 32 + e >= lim_local) sr[c][e] = __float_as_uint(-INFINITY);
       }
-      // row maximum: four independent 3-input max chains
-      float a0 = fmaxf(__uint_as_float(sr[0][0]), __uint_as_float(sr[0][1]));
-      float a1 = fmaxf(__uint_as_float(sr[0][2]), __uint_as_float(sr[0][3]));
-      float a2 = fmaxf(__uint_as_float(sr[0][4]), __uint_as_float(sr[0][5]));
-      float a3 = fmaxf(__uint_as_float(sr[0][6]), __uint_as_float(sr[0][7]));
+      // row maximum: eight independent 3-input max chains, then a small tree
+      float am[8];
 #pragma unroll
-      for (int i = 8; i < 128; i += 8) {
-        a0 = ptx::max3(a0, __uint_as_float(sr[i >> 5][(i + 0) & 31]), __uint_as_float(sr[i >> 5][(i + 1) & 31]));
-        a1 = ptx::max3(a1, __uint_as_float(sr[i >> 5][(i + 2) & 31]), __uint_as_float(sr[i >> 5][(i + 3) & 31]));
-        a2 = ptx::max3(a2, __uint_as_float(sr[i >> 5][(i + 4) & 31]), __uint_as_float(sr[i >> 5][(i + 5) & 31]));
-        a3 = ptx::max3(a3, __uint_as_float(sr[i >> 5][(i + 6) & 31]), __uint_as_float(sr[i >> 5][(i + 7) & 31]));
-      }
-      const float mx = ptx::max3(a0, a1, fmaxf(a2, a3));
+      for (int k = 0; k < 8; ++k) am[k] = fmaxf(__uint_as_float(sr[0][2 * k]), __uint_as_float(sr[0][2 * k + 1]));
+#pragma unroll
+      for (int i = 16; i < 128; i += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          am[k] = ptx::max3(am[k], __uint_as_float(sr[i >> 5][(i + 2 * k) & 31]),
+                            __uint_as_float(sr[i >> 5][(i + 2 * k + 1) & 31]));
+      const float mx = ptx::max3(ptx::max3(am[0], am[1], am[2]), ptx::max3(am[3], am[4], am[5]),
+                                 fmaxf(am[6], am[7]));
       const float m_tile = mx * sl2;  // -inf stays -inf
       bool rescale = false;
       float factor = 1.0f;
@@ -458,6 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         l *= factor;
       }
       if (__any_sync(0xffffffffu, rescale)) {
+        if (!(ok = wait_pv())) break;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -472,12 +566,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t negm2 = ptx::f2_pack(-m_use, -m_use);
       uint64_t sum_a = ptx::f2_pack(0.0f, 0.0f), sum_b = sum_a;
       // keys 0..63: P released early so the PV product can start on them
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t pk[16];
-        exp_pack32(sr[c], sl2x2, negm2, pk, sum_a, sum_b);
-        ptx::tmem_st16(tS + c * 16, pk);
-      }
+      uint32_t pk0[16], pk1[16];
+      exp_pack32(sr[0], sl2x2, negm2, pk0, sum_a, sum_b);
+      exp_pack32(sr[1], sl2x2, negm2, pk1, sum_a, sum_b);
+      if (!(ok = wait_pv())) break;
+      ptx::tmem_st16(tP, pk0);
+      ptx::tmem_st16(tP + 16, pk1);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
@@ -487,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 2; c < 4; ++c) {
         uint32_t pk[16];
         exp_pack32(sr[c], sl2x2, negm2, pk, sum_a, sum_b);
-        ptx::tmem_st16(tS + c * 16, pk);
+        ptx::tmem_st16(tP + c * 16, pk);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
