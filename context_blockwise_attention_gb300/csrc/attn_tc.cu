@@ -8,27 +8,34 @@
 // chunks are combined by the merge kernel.
 //
 // How (GB300 design, not the pages'):
-//   * One CTA = two 128-row Q tiles (A, B) of one head.  KV tiles are 128 keys.
-//   * warp 0: TMA producer (Q once; K and V tiles through a ring of shared-memory stages,
-//     128-byte swizzled).  warp 1: allocates tensor memory and issues tcgen05.mma from one
-//     thread.  warps 4-7 / 8-11: softmax warpgroups for Q tiles A / B, one thread per row.
+//   * Persistent: one CTA per SM walks a list of units -- a pair of 128-row Q tiles (A, B) of
+//     one head -- in longest-first order, snaking across CTAs round by round (causal units
+//     shrink towards the start of the shard); Q heads of one KV group are adjacent so their
+//     K/V tiles are shared through L2.  KV tiles are 128 keys.
+//   * warp 0: TMA producer.  K and V tiles stream through rings of shared-memory stages
+//     (128-byte swizzle) straight across unit boundaries; a unit's Q is loaded as soon as the
+//     previous unit's last QK has completed.  warp 1: allocates tensor memory and issues
+//     tcgen05.mma (whole warp waits, one elected lane issues).  warps 4-7 / 8-11: softmax
+//     warpgroups for Q tiles A / B, one thread per row.
 //   * Tensor memory (512 columns): S_A, S_B (128 fp32 columns each), O_A, O_B (D columns).
-//     P (bf16) is written back over the first 64 columns of its S tile and fed to the PV
-//     product straight from tensor memory.
-//   * The tensor pipe runs QK_A(j), PV_B(j-1), QK_B(j), PV_A(j): each softmax warpgroup has two
-//     MMA slots to turn its S tile into P while the other tile keeps the tensor core busy.
+//     P (bf16) is written over the first 64 columns of its S tile and fed to the PV product
+//     from tensor memory.
+//   * Tensor-pipe order per KV step j: QK_A(j), PV_B(j-1), QK_B(j), PV_A(j); each softmax
+//     warpgroup has two MMA slots to turn its S tile into P, and releases P in two halves so the
+//     PV product starts on keys 0..63 while 64..127 are still being exponentiated.
 //   * Online softmax in base 2 with a lazy rescale: O and l are rescaled only when a row's
 //     maximum grows by more than 2^8; otherwise exponentials use the stale maximum.  The final
 //     O / l and LSE use that same reference, so the result is exact.
 //   * Causal visibility is by global position: key j is visible to query i iff
-//     kv_pos(j) <= q_pos(i).  KV tiles entirely in the future of the CTA's last row are never
+//     kv_pos(j) <= q_pos(i).  KV tiles entirely in the future of a unit's last row are never
 //     loaded or multiplied; only tiles that straddle the boundary (or the ragged end of the
 //     chunk) are masked element by element.
-//   * CTAs are ordered longest-first (the hardware block scheduler then balances the causal
-//     triangle), with the Q heads of one KV group adjacent so their K/V tiles are shared in L2.
+//   * Epilogue: after a unit's last PV the softmax warpgroup copies O into registers, releases
+//     its tensor memory (the next unit's PV may start) and streams O / l through a 16 KB
+//     swizzled staging box per warpgroup with TMA bulk stores (rows past sq are clipped).
 //   * Every mbarrier wait is bounded by %globaltimer; on expiry the kernel records
-//     CP_ERR_TIMEOUT in the caller's status word, every role leaves its loop, outstanding TMA
-//     loads and MMAs are drained and tensor memory is freed before the CTA exits.
+//     CP_ERR_TIMEOUT in the caller's status word, every role leaves its loops, outstanding TMA
+//     loads, MMAs and bulk stores are drained and tensor memory is freed before the CTA exits.
 #include <math.h>
 
 #include <cuda.h>
@@ -56,8 +63,8 @@ enum WaitSite : int {
   kSitePFull = 7,
   kSiteOFinal = 8,
   kSiteTest = 9,
-  kSiteSFree = 10,
-  kSitePvDone = 11,
+  kSiteQEmpty = 10,
+  kSiteOEmpty = 11,
 };
 
 struct TcParams {
@@ -67,6 +74,7 @@ struct TcParams {
   int64_t sq, skv;
   int32_t hq, hkv, group;
   int32_t n_pairs;
+  int64_t n_units;  // n_pairs * hq
   int32_t causal, o_bf16, descending, test_stall;
   float scale_log2;
   int64_t q_base, q_stride, k_base, k_stride;
@@ -82,33 +90,29 @@ struct Layout {
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
-  // barriers: q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_half[2],
-  //           p_full[2], o_final[2], s_free[2], pv_done[2], never, drain
-  static constexpr int kNumBars = 1 + 4 * kStages + 12 + 2;
-  // Tensor memory: S_A, S_B at columns 0 / 128.  D=128: O_A, O_B at 256 / 384 and P written over
-  // the first 64 columns of its S tile.  D=64: O_A, O_B at 256 / 320 and separate P_A, P_B at
-  // 384 / 448, so a tile's S can be overwritten by the next QK while its P still feeds the PV
-  // product ("decoupled P").
-  static constexpr bool kSepP = (D == 64);
-  static constexpr uint32_t kColO = 256, kStrideO = kSepP ? 64 : 128;
-  static constexpr uint32_t kColP = kSepP ? 384 : 0, kStrideP = kSepP ? 64 : 128;
+  static constexpr int kOffStage = kOffV + kStages * kTileBytes;  // 16 KB box per warpgroup
+  static constexpr int kOffBar = kOffStage + 2 * kChunkBytes;
+  // barriers: q_full, q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2],
+  //           p_half[2], p_full[2], o_final[2], o_empty[2], never, drain
+  static constexpr int kNumBars = 2 + 4 * kStages + 10 + 2;
   static constexpr int kOffCtl = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffCtl + 16;
   static constexpr int kSmemLaunch = kBytes + 1024;  // slack for 1024-byte alignment
+  static constexpr int kBoxesF32 = D / 32;           // 32 fp32 columns per 128-byte box
+  static constexpr int kBoxesBf16 = D / 64;          // 64 bf16 columns per box
 };
+static_assert(Layout<128>::kSmemLaunch <= 232448, "shared memory budget (D=128)");
 
 // Register split (setmaxnreg): the TMA/MMA warpgroup gives registers to the two softmax
-// warpgroups.  4 warps x 56 + 8 warps x 224 = 12 warps x 168, the launch's allocation.
+// warpgroups.  4 warps x 88 + 8 warps x 208 = 12 warps x 168, the launch's allocation.
 constexpr uint32_t kRegsControl = 88;
 constexpr uint32_t kRegsSoftmax = 208;
 static_assert(4 * kRegsControl + 8 * kRegsSoftmax == 12 * 168, "register split must match launch");
 
 struct Bars {
-  uint32_t q_full;
+  uint32_t q_full, q_empty;
   uint32_t k_full, k_empty, v_full, v_empty;  // stage 0; +8 per stage
-  uint32_t s_full, p_half, p_full, o_final;   // tile A; +8 for tile B
-  uint32_t s_free, pv_done;                   // tile A; +8 for tile B (decoupled P only)
+  uint32_t s_full, p_half, p_full, o_final, o_empty;  // tile A; +8 for tile B
   uint32_t never, drain;
 };
 
@@ -126,8 +130,6 @@ __device__ __forceinline__ void raise_abort(const Ctl& c, int site) {
 // Waits for phase `parity` of `bar`; gives up (returns false) when the kernel is aborting or
 // when the wait exceeds the time limit, in which case it starts the abort itself.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Ctl& c, int site) {
-  // a phase that has already completed is seen by the non-blocking test at once; try_wait may
-  // suspend the thread for a time slice even then
   if (ptx::mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer();
   for (uint32_t it = 1;; ++it) {
@@ -164,6 +166,34 @@ __device__ __forceinline__ int64_t visible_keys(const TcParams& p, int64_t row) 
   return n < p.skv ? n : p.skv;
 }
 
+// The k-th unit of CTA b: rounds of `grid` units, forward on even rounds, backward on odd ones.
+__device__ __forceinline__ int64_t unit_of(int64_t k, int64_t b, int64_t grid) {
+  return k * grid + ((k & 1) ? (grid - 1 - b) : b);
+}
+
+struct Unit {
+  int64_t row0;  // first query row of tile A
+  int h, kvh;
+  int n_tiles;
+};
+
+// Units are numbered longest first: pairs in decreasing order when causal, heads innermost.
+__device__ __forceinline__ Unit decode_unit(const TcParams& p, int64_t u) {
+  Unit w;
+  const int64_t pair = p.causal ? (p.n_pairs - 1 - u / p.hq) : (u / p.hq);
+  w.h = static_cast<int>(u % p.hq);
+  w.kvh = w.h / p.group;
+  w.row0 = pair * (2 * kRows);
+  int64_t n_keys = p.skv;
+  if (p.causal) {
+    int64_t last = w.row0 + 2 * kRows - 1;
+    if (last > p.sq - 1) last = p.sq - 1;
+    n_keys = visible_keys(p, last);
+  }
+  w.n_tiles = static_cast<int>((n_keys + kKeys - 1) / kKeys);
+  return w;
+}
+
 // exp2 of 32 scaled scores (x = s * sl2 - m) packed to 16 bf16 pairs; adds the fp32 values to
 // the two packed partial sums.  (Evaluating part of the exponentials with a polynomial on the FMA
 // pipe was measured slower on GB300 for both head dims: the softmax is bound by instruction issue
@@ -198,24 +228,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = ptx::smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // ---- the work unit: a pair of Q tiles of one head, longest first when causal
-  const int64_t u = blockIdx.x;
-  const int64_t pair = p.causal ? (p.n_pairs - 1 - u / p.hq) : (u / p.hq);
-  const int h = static_cast<int>(u % p.hq);
-  const int kvh = h / p.group;
-  const int64_t row0 = pair * (2 * kRows);
-  int64_t n_keys = p.skv;
-  if (p.causal) {
-    int64_t last = row0 + 2 * kRows - 1;
-    if (last > p.sq - 1) last = p.sq - 1;
-    n_keys = visible_keys(p, last);
-  }
-  const int n_tiles = static_cast<int>((n_keys + kKeys - 1) / kKeys);
+  const int64_t cta = blockIdx.x;
+  const int64_t grid = gridDim.x;
 
   Bars b;
   b.q_full = sbase + L::kOffBar;
-  b.k_full = b.q_full + 8;
+  b.q_empty = b.q_full + 8;
+  b.k_full = b.q_empty + 8;
   b.k_empty = b.k_full + 8 * L::kStages;
   b.v_full = b.k_empty + 8 * L::kStages;
   b.v_empty = b.v_full + 8 * L::kStages;
@@ -223,9 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   b.p_half = b.s_full + 16;
   b.p_full = b.p_half + 16;
   b.o_final = b.p_full + 16;
-  b.s_free = b.o_final + 16;
-  b.pv_done = b.s_free + 16;
-  b.never = b.pv_done + 16;
+  b.o_empty = b.o_final + 16;
+  b.never = b.o_empty + 16;
   b.drain = b.never + 8;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffCtl);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffCtl + 4);
@@ -234,6 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     ptx::mbar_init(b.q_full, 1);
+    ptx::mbar_init(b.q_empty, 1);
     for (int s = 0; s < L::kStages; ++s) {
       ptx::mbar_init(b.k_full + 8 * s, 1);
       ptx::mbar_init(b.k_empty + 8 * s, 1);
@@ -245,8 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(b.p_half + 8 * t, 4);
       ptx::mbar_init(b.p_full + 8 * t, 4);
       ptx::mbar_init(b.o_final + 8 * t, 1);
-      ptx::mbar_init(b.s_free + 8 * t, 4);
-      ptx::mbar_init(b.pv_done + 8 * t, 1);
+      ptx::mbar_init(b.o_empty + 8 * t, 4);
     }
     ptx::mbar_init(b.never, 1);
     ptx::mbar_init(b.drain, 1);
@@ -267,209 +285,188 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     ptx::regs_dec<kRegsControl>();
-  if (warp == 0 && n_tiles > 0) {
-    // ================================================================ TMA producer
-    const bool leader = ptx::elect_one();
-    if (leader) {
-      ptx::tma_prefetch_desc(&tm_q);
-      ptx::tma_prefetch_desc(&tm_k);
-      ptx::tma_prefetch_desc(&tm_v);
-      ptx::mbar_arrive_expect_tx(b.q_full, 2 * L::kTileBytes);
-      for (int x = 0; x < 2; ++x)
-        for (int c = 0; c < L::kChunks; ++c)
-          ptx::tma_load_2d(sQ + x * L::kTileBytes + c * L::kChunkBytes, &tm_q, h * D + c * 64,
-                           static_cast<int32_t>(row0 + x * kRows), b.q_full);
-    }
-    __syncwarp();
-    int issued_k = 0, issued_v = 0;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int t = p.descending ? n_tiles - 1 - j : j;
-      const int st = j % L::kStages;
-      const uint32_t ph = (j / L::kStages) & 1;
-      if (!wait_warp(b.k_empty + 8 * st, ph ^ 1, ctl, kSiteKEmpty)) break;
+    if (warp == 0) {
+      // ============================================================== TMA producer
+      const bool leader = ptx::elect_one();
       if (leader) {
-        ptx::mbar_arrive_expect_tx(b.k_full + 8 * st, L::kTileBytes);
-        for (int c = 0; c < L::kChunks; ++c)
-          ptx::tma_load_2d(sK + st * L::kTileBytes + c * L::kChunkBytes, &tm_k, kvh * D + c * 64,
-                           t * kKeys, b.k_full + 8 * st);
+        ptx::tma_prefetch_desc(&tm_q);
+        ptx::tma_prefetch_desc(&tm_k);
+        ptx::tma_prefetch_desc(&tm_v);
       }
-      __syncwarp();
-      issued_k = j + 1;
-      if (!wait_warp(b.v_empty + 8 * st, ph ^ 1, ctl, kSiteVEmpty)) break;
-      if (leader) {
-        ptx::mbar_arrive_expect_tx(b.v_full + 8 * st, L::kTileBytes);
-        for (int c = 0; c < L::kChunks; ++c)
-          ptx::tma_load_2d(sV + st * L::kTileBytes + c * L::kChunkBytes, &tm_v, kvh * D + c * 64,
-                           t * kKeys, b.v_full + 8 * st);
-      }
-      __syncwarp();
-      issued_v = j + 1;
-    }
-    if (*abort_flag && leader) {
-      // copies in flight must land before the CTA's shared memory goes away
-      wait_drain(b.q_full, 0, p.timeout_ns);
-      for (int s = 0; s < L::kStages; ++s) {
-        const int last_k = ((issued_k - 1 - s) >= 0) ? issued_k - 1 - ((issued_k - 1 - s) % L::kStages) : -1;
-        if (last_k >= 0) wait_drain(b.k_full + 8 * s, (last_k / L::kStages) & 1, p.timeout_ns);
-        const int last_v = ((issued_v - 1 - s) >= 0) ? issued_v - 1 - ((issued_v - 1 - s) % L::kStages) : -1;
-        if (last_v >= 0) wait_drain(b.v_full + 8 * s, (last_v / L::kStages) & 1, p.timeout_ns);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ================================================================ MMA issuer
-    // The whole warp runs the loop and waits; one elected lane issues each tcgen05 instruction.
-    const bool leader = ptx::elect_one();
-    constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(kRows, kKeys, 0, 0);
-    constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kRows, D, 0, 1);
-    // descriptor bases (start address field counts 16-byte units)
-    const uint64_t dQ0 = ptx::smem_desc_sw128(sQ, 16, 1024);
-    const uint64_t dK0 = ptx::smem_desc_sw128(sK, 16, 1024);
-    const uint64_t dV0 = ptx::smem_desc_sw128(sV, L::kChunkBytes, 1024);
-    constexpr uint64_t kTileUnits = L::kTileBytes >> 4;
-    bool ok = true;
-    if (p.test_stall && blockIdx.x == 0) ok = wait_warp(b.never, 0, ctl, kSiteTest);
-    if (ok && n_tiles > 0) ok = wait_warp(b.q_full, 0, ctl, kSiteQ);
-
-    auto issue_qk = [&](int x, int st) {
-      const uint64_t qd = dQ0 + x * kTileUnits;
-      const uint64_t kd = dK0 + st * kTileUnits;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t off = static_cast<uint64_t>(((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4);
-        ptx::mma_ss(tmem + x * 128u, qd + off, kd + off, kIdescQK, kk > 0 ? 1u : 0u);
-      }
-    };
-    auto issue_pv = [&](int x, int st, int half, bool acc) {
-      const uint64_t vd = dV0 + st * kTileUnits;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int kk = half * 4 + q;
-        ptx::mma_ts(tmem + L::kColO + x * L::kStrideO, tmem + L::kColP + x * L::kStrideP + kk * 8,
-                    vd + static_cast<uint64_t>(kk * 128), kIdescPV, (acc || kk > 0) ? 1u : 0u);
-      }
-    };
-    // PV for Q tile x on stage st: first half as soon as P's first 64 keys are in tensor memory
-    auto pv_tile = [&](int x, int st, int jj) -> bool {
-      if (!wait_warp(b.p_half + 8 * x, jj & 1, ctl, kSitePFull)) return false;
-      ptx::tc_fence_after();
-      if (leader) issue_pv(x, st, 0, jj > 0);
-      __syncwarp();
-      if (!wait_warp(b.p_full + 8 * x, jj & 1, ctl, kSitePFull)) return false;
-      ptx::tc_fence_after();
-      if (leader) issue_pv(x, st, 1, true);
-      __syncwarp();
-      return true;
-    };
-
-    if constexpr (L::kSepP) {
-      // QK_A(j), QK_B(j) as soon as the softmax warpgroups have copied S(j-1) to registers; the
-      // PV products of step j-1 follow, each gated by its P.
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int st = j % L::kStages;
-        const uint32_t ph = (j / L::kStages) & 1;
-        if (!(ok = wait_warp(b.k_full + 8 * st, ph, ctl, kSiteKFull))) break;
-        if (j > 0 && !(ok = wait_warp(b.s_free, (j - 1) & 1, ctl, kSiteSFree))) break;
-        ptx::tc_fence_after();
-        if (leader) {
-          issue_qk(0, st);
-          ptx::mma_commit(b.s_full);
-        }
-        __syncwarp();
-        if (j > 0 && !(ok = wait_warp(b.s_free + 8, (j - 1) & 1, ctl, kSiteSFree))) break;
-        ptx::tc_fence_after();
-        if (leader) {
-          issue_qk(1, st);
-          ptx::mma_commit(b.s_full + 8);
-          ptx::mma_commit(b.k_empty + 8 * st);
-        }
-        __syncwarp();
-        if (j > 0) {
-          const int pj = j - 1;
-          const int pst = pj % L::kStages;
-          if (!(ok = wait_warp(b.v_full + 8 * pst, (pj / L::kStages) & 1, ctl, kSiteVFull))) break;
-          if (!(ok = pv_tile(0, pst, pj))) break;
-          if (leader) ptx::mma_commit(b.pv_done);
-          __syncwarp();
-          if (!(ok = pv_tile(1, pst, pj))) break;
+      int64_t g = 0;        // global KV-tile counter (ring stage / phase)
+      int64_t kq = 0;       // units with work seen so far (Q buffer phase)
+      int64_t kl = 0, vl = 0, ql = 0;  // K, V, Q loads issued
+      bool ok = true;
+      for (int64_t k = 0; ok; ++k) {
+        const int64_t u = unit_of(k, cta, grid);
+        if (u >= p.n_units) break;
+        const Unit w = decode_unit(p, u);
+        if (w.n_tiles == 0) continue;
+        for (int j = 0; ok && j < w.n_tiles; ++j) {
+          const int t = p.descending ? w.n_tiles - 1 - j : j;
+          const int64_t gj = g + j;
+          const int st = static_cast<int>(gj % L::kStages);
+          const uint32_t ph = static_cast<uint32_t>((gj / L::kStages) & 1);
+          if (!(ok = wait_warp(b.k_empty + 8 * st, ph ^ 1, ctl, kSiteKEmpty))) break;
           if (leader) {
-            ptx::mma_commit(b.pv_done + 8);
-            ptx::mma_commit(b.v_empty + 8 * pst);
+            ptx::mbar_arrive_expect_tx(b.k_full + 8 * st, L::kTileBytes);
+            for (int c = 0; c < L::kChunks; ++c)
+              ptx::tma_load_2d(sK + st * L::kTileBytes + c * L::kChunkBytes, &tm_k, w.kvh * D + c * 64,
+                               t * kKeys, b.k_full + 8 * st);
           }
           __syncwarp();
-        }
-      }
-      if (ok && n_tiles > 0) {
-        const int pj = n_tiles - 1;
-        const int pst = pj % L::kStages;
-        ok = wait_warp(b.v_full + 8 * pst, (pj / L::kStages) & 1, ctl, kSiteVFull);
-        if (ok && (ok = pv_tile(0, pst, pj))) {
-          if (leader) {
-            ptx::mma_commit(b.pv_done);
-            ptx::mma_commit(b.o_final);
-          }
-          __syncwarp();
-          if ((ok = pv_tile(1, pst, pj))) {
+          kl = gj + 1;
+          if (j == 0) {
+            // the Q buffer is free once every QK of the previous unit has completed
+            if (kq > 0 && !(ok = wait_warp(b.q_empty, static_cast<uint32_t>((kq - 1) & 1), ctl, kSiteQEmpty)))
+              break;
             if (leader) {
-              ptx::mma_commit(b.pv_done + 8);
-              ptx::mma_commit(b.v_empty + 8 * pst);
-              ptx::mma_commit(b.o_final + 8);
+              ptx::mbar_arrive_expect_tx(b.q_full, 2 * L::kTileBytes);
+              for (int x = 0; x < 2; ++x)
+                for (int c = 0; c < L::kChunks; ++c)
+                  ptx::tma_load_2d(sQ + x * L::kTileBytes + c * L::kChunkBytes, &tm_q, w.h * D + c * 64,
+                                   static_cast<int32_t>(w.row0 + x * kRows), b.q_full);
             }
+            __syncwarp();
+            ql = kq + 1;
+          }
+          if (!(ok = wait_warp(b.v_empty + 8 * st, ph ^ 1, ctl, kSiteVEmpty))) break;
+          if (leader) {
+            ptx::mbar_arrive_expect_tx(b.v_full + 8 * st, L::kTileBytes);
+            for (int c = 0; c < L::kChunks; ++c)
+              ptx::tma_load_2d(sV + st * L::kTileBytes + c * L::kChunkBytes, &tm_v, w.kvh * D + c * 64,
+                               t * kKeys, b.v_full + 8 * st);
+          }
+          __syncwarp();
+          vl = gj + 1;
+        }
+        g += w.n_tiles;
+        kq += 1;
+      }
+      if (*abort_flag && leader) {
+        // copies in flight must land before the CTA's shared memory goes away: wait (bounded)
+        // for the last load issued into every stage, and for the last Q load
+        if (ql > 0) wait_drain(b.q_full, static_cast<uint32_t>((ql - 1) & 1), p.timeout_ns);
+        for (int s = 0; s < L::kStages; ++s) {
+          const int64_t lk = (kl - 1 - s >= 0) ? kl - 1 - ((kl - 1 - s) % L::kStages) : -1;
+          if (lk >= 0) wait_drain(b.k_full + 8 * s, static_cast<uint32_t>((lk / L::kStages) & 1), p.timeout_ns);
+          const int64_t lv = (vl - 1 - s >= 0) ? vl - 1 - ((vl - 1 - s) % L::kStages) : -1;
+          if (lv >= 0) wait_drain(b.v_full + 8 * s, static_cast<uint32_t>((lv / L::kStages) & 1), p.timeout_ns);
+        }
+      }
+      __syncwarp();
+    } else if (warp == 1) {
+      // ============================================================== MMA issuer
+      // The whole warp runs the loop and waits; one elected lane issues each tcgen05 instruction.
+      const bool leader = ptx::elect_one();
+      constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(kRows, kKeys, 0, 0);
+      constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kRows, D, 0, 1);
+      // descriptor bases (start address field counts 16-byte units)
+      const uint64_t dQ0 = ptx::smem_desc_sw128(sQ, 16, 1024);
+      const uint64_t dK0 = ptx::smem_desc_sw128(sK, 16, 1024);
+      const uint64_t dV0 = ptx::smem_desc_sw128(sV, L::kChunkBytes, 1024);
+      constexpr uint64_t kTileUnits = L::kTileBytes >> 4;
+      bool ok = true;
+      if (p.test_stall && blockIdx.x == 0) ok = wait_warp(b.never, 0, ctl, kSiteTest);
+
+      auto issue_qk = [&](int x, int st) {
+        const uint64_t qd = dQ0 + x * kTileUnits;
+        const uint64_t kd = dK0 + st * kTileUnits;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4);
+          ptx::mma_ss(tmem + x * 128u, qd + off, kd + off, kIdescQK, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int x, int st, int half, bool acc) {
+        const uint64_t vd = dV0 + st * kTileUnits;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int kk = half * 4 + q;
+          ptx::mma_ts(tmem + 256u + x * 128u, tmem + x * 128u + kk * 8, vd + static_cast<uint64_t>(kk * 128),
+                      kIdescPV, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      // PV for Q tile x with the V tile of global step gg (stage st): first half as soon as P's
+      // first 64 keys are in tensor memory.  `first` = first PV of the unit (overwrites O), which
+      // waits until the previous unit's epilogue has copied O out (o_empty).
+      auto pv_tile = [&](int x, int st, int64_t gg, bool first, int64_t kq) -> bool {
+        if (first && kq > 0 &&
+            !wait_warp(b.o_empty + 8 * x, static_cast<uint32_t>((kq - 1) & 1), ctl, kSiteOEmpty))
+          return false;
+        if (!wait_warp(b.p_half + 8 * x, static_cast<uint32_t>(gg & 1), ctl, kSitePFull)) return false;
+        ptx::tc_fence_after();
+        if (leader) issue_pv(x, st, 0, !first);
+        __syncwarp();
+        if (!wait_warp(b.p_full + 8 * x, static_cast<uint32_t>(gg & 1), ctl, kSitePFull)) return false;
+        ptx::tc_fence_after();
+        if (leader) issue_pv(x, st, 1, true);
+        __syncwarp();
+        return true;
+      };
+
+      int64_t g = 0, kq = 0;
+      for (int64_t k = 0; ok; ++k) {
+        const int64_t u = unit_of(k, cta, grid);
+        if (u >= p.n_units) break;
+        const Unit w = decode_unit(p, u);
+        if (w.n_tiles == 0) continue;
+        if (!(ok = wait_warp(b.q_full, static_cast<uint32_t>(kq & 1), ctl, kSiteQ))) break;
+        const int n = w.n_tiles;
+        for (int j = 0; j < n; ++j) {
+          const int64_t gj = g + j;
+          const int st = static_cast<int>(gj % L::kStages);
+          const uint32_t ph = static_cast<uint32_t>((gj / L::kStages) & 1);
+          if (!(ok = wait_warp(b.k_full + 8 * st, ph, ctl, kSiteKFull))) break;
+          ptx::tc_fence_after();
+          if (leader) {
+            issue_qk(0, st);
+            ptx::mma_commit(b.s_full);
+          }
+          __syncwarp();
+          if (j > 0) {
+            const int pst = static_cast<int>((gj - 1) % L::kStages);
+            if (!(ok = pv_tile(1, pst, gj - 1, j - 1 == 0, kq))) break;
+            if (leader) ptx::mma_commit(b.v_empty + 8 * pst);
+            __syncwarp();
+          }
+          if (leader) {
+            issue_qk(1, st);
+            ptx::mma_commit(b.s_full + 8);
+            ptx::mma_commit(b.k_empty + 8 * st);
+            if (j == n - 1) ptx::mma_commit(b.q_empty);  // every QK of this unit issued
+          }
+          __syncwarp();
+          if (!(ok = wait_warp(b.v_full + 8 * st, ph, ctl, kSiteVFull))) break;
+          if (!(ok = pv_tile(0, st, gj, j == 0, kq))) break;
+          if (j == n - 1) {
+            if (leader) ptx::mma_commit(b.o_final);
             __syncwarp();
           }
         }
-      }
-    } else {
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int st = j % L::kStages;
-        const uint32_t ph = (j / L::kStages) & 1;
-        if (!(ok = wait_warp(b.k_full + 8 * st, ph, ctl, kSiteKFull))) break;
-        ptx::tc_fence_after();
-        if (leader) {
-          issue_qk(0, st);
-          ptx::mma_commit(b.s_full);
-        }
-        __syncwarp();
-        if (j > 0) {
-          const int pst = (j - 1) % L::kStages;
-          if (!(ok = pv_tile(1, pst, j - 1))) break;
-          if (leader) ptx::mma_commit(b.v_empty + 8 * pst);
-          __syncwarp();
-        }
-        if (leader) {
-          issue_qk(1, st);
-          ptx::mma_commit(b.s_full + 8);
-          ptx::mma_commit(b.k_empty + 8 * st);
-        }
-        __syncwarp();
-        if (!(ok = wait_warp(b.v_full + 8 * st, ph, ctl, kSiteVFull))) break;
-        if (!(ok = pv_tile(0, st, j))) break;
-        if (j == n_tiles - 1) {
-          if (leader) ptx::mma_commit(b.o_final);
-          __syncwarp();
-        }
-      }
-      if (ok && n_tiles > 0) {
-        const int j = n_tiles - 1;
-        const int st = j % L::kStages;
-        if ((ok = pv_tile(1, st, j))) {
+        if (!ok) break;
+        {
+          const int64_t gl = g + n - 1;
+          const int st = static_cast<int>(gl % L::kStages);
+          if (!(ok = pv_tile(1, st, gl, n == 1, kq))) break;
           if (leader) {
             ptx::mma_commit(b.v_empty + 8 * st);
             ptx::mma_commit(b.o_final + 8);
           }
           __syncwarp();
         }
+        g += n;
+        kq += 1;
+      }
+      if (!ok) {
+        // every MMA issued so far must complete before tensor memory is released
+        if (leader) {
+          ptx::mma_commit(b.drain);
+          wait_drain(b.drain, 0, p.timeout_ns);
+        }
+        __syncwarp();
       }
     }
-    if (!ok) {
-      // every MMA issued so far must complete before tensor memory is released
-      if (leader) {
-        ptx::mma_commit(b.drain);
-        wait_drain(b.drain, 0, p.timeout_ns);
-      }
-      __syncwarp();
-    }
-  }
   } else {
     ptx::regs_inc<kRegsSoftmax>();
     // ================================================================ softmax warpgroups
@@ -478,186 +475,183 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = wq * 32 + lane;            // row inside the tile
     const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + x * 128u + lane_bits;
-    const uint32_t tO = tmem + L::kColO + x * L::kStrideO + lane_bits;
-    const uint32_t tP = tmem + L::kColP + x * L::kStrideP + lane_bits;
-    const int64_t tile_row0 = row0 + x * kRows;
-    const int64_t grow = tile_row0 + r;
-    const int64_t lim = p.causal ? visible_keys(p, grow) : p.skv;
-    const int64_t q_first = p.q_base + p.q_stride * tile_row0;
+    const uint32_t tO = tmem + 256u + x * 128u + lane_bits;
+    const uint32_t stage = sbase + L::kOffStage + static_cast<uint32_t>(x) * L::kChunkBytes;
+    const uint32_t row_addr = stage + static_cast<uint32_t>(r) * 128u;
+    const uint32_t sw = static_cast<uint32_t>(r & 7);
+    const bool store_leader = (wq == 0 && lane == 0);
     const float sl2 = p.scale_log2;
     const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
-
-    float m_ref = -INFINITY;  // running maximum (log2 units of scaled scores)
-    float l = 0.0f;           // running sum of 2^(x - m_ref)
     bool ok = true;
+    bool staged = false;  // a bulk store from the staging box may still be reading it
+    int64_t g = 0, kq = 0;
 
-    for (int j = 0; j < n_tiles; ++j) {
-      const int t = p.descending ? n_tiles - 1 - j : j;
-      if (!(ok = wait_warp(b.s_full + 8 * x, j & 1, ctl, kSiteSFull))) break;
-      ptx::tc_fence_after();
-      uint32_t sr[4][32];
+    for (int64_t k = 0;; ++k) {
+      const int64_t u = unit_of(k, cta, grid);
+      if (u >= p.n_units) break;
+      const Unit w = decode_unit(p, u);
+      const int64_t tile_row0 = w.row0 + x * kRows;
+      const int64_t grow = tile_row0 + r;
+      const int64_t lim = p.causal ? visible_keys(p, grow) : p.skv;
+      const int64_t q_first = p.q_base + p.q_stride * tile_row0;
+      float m_ref = -INFINITY;  // running maximum (log2 units of scaled scores)
+      float l = 0.0f;           // running sum of 2^(x - m_ref)
+
+      for (int j = 0; j < w.n_tiles; ++j) {
+        const int t = p.descending ? w.n_tiles - 1 - j : j;
+        const int64_t gj = g + j;
+        if (!(ok = wait_warp(b.s_full + 8 * x, static_cast<uint32_t>(gj & 1), ctl, kSiteSFull))) break;
+        ptx::tc_fence_after();
+        uint32_t sr[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + c * 32, sr[c]);
-      ptx::tmem_wait_ld();
-      // decoupled P: S is in registers, the next QK may overwrite it
-      bool pv_seen = true;
-      if constexpr (L::kSepP) {
+        for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + c * 32, sr[c]);
+        ptx::tmem_wait_ld();
+
+        const int64_t k0 = static_cast<int64_t>(t) * kKeys;
+        const bool need_mask =
+            (k0 + kKeys > p.skv) || (p.causal && p.k_base + p.k_stride * (k0 + kKeys - 1) > q_first);
+        if (need_mask) {
+          const int64_t lim_local = lim - k0;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (c * 32 + e >= lim_local) sr[c][e] = __float_as_uint(-INFINITY);
+        }
+        // row maximum: eight independent 3-input max chains, then a small tree
+        float am[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) am[q] = fmaxf(__uint_as_float(sr[0][2 * q]), __uint_as_float(sr[0][2 * q + 1]));
+#pragma unroll
+        for (int i = 16; i < 128; i += 16)
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            am[q] = ptx::max3(am[q], __uint_as_float(sr[i >> 5][(i + 2 * q) & 31]),
+                              __uint_as_float(sr[i >> 5][(i + 2 * q + 1) & 31]));
+        const float mx = ptx::max3(ptx::max3(am[0], am[1], am[2]), ptx::max3(am[3], am[4], am[5]),
+                                   fmaxf(am[6], am[7]));
+        const float m_tile = mx * sl2;  // -inf stays -inf
+        bool rescale = false;
+        float factor = 1.0f;
+        if (m_ref == -INFINITY) {
+          m_ref = m_tile;  // first visible keys: O and l are still zero
+        } else if (m_tile > m_ref + kRescaleThreshold) {
+          rescale = true;
+          factor = ptx::ex2(m_ref - m_tile);
+          m_ref = m_tile;
+          l *= factor;
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            ptx::tmem_ld32(tO + c * 32, o);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
+            ptx::tmem_st32(tO + c * 32, o);
+          }
+        }
+        const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
+        const uint64_t negm2 = ptx::f2_pack(-m_use, -m_use);
+        uint64_t sum_a = ptx::f2_pack(0.0f, 0.0f), sum_b = sum_a;
+        // keys 0..63: P released early so the PV product can start on them
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t pk[16];
+          exp_pack32(sr[c], sl2x2, negm2, pk, sum_a, sum_b);
+          ptx::tmem_st16(tS + c * 16, pk);
+        }
+        ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(b.s_free + 8 * x);
-        pv_seen = (j == 0);
-      }
-      // decoupled P: O and P_x may only be touched once PV_x(j-1) has completed
-      auto wait_pv = [&]() -> bool {
-        if (pv_seen) return true;
-        pv_seen = true;
-        if (!wait_warp(b.pv_done + 8 * x, (j - 1) & 1, ctl, kSitePvDone)) return false;
-        ptx::tc_fence_after();
-        return true;
-      };
-
-      const int64_t k0 = static_cast<int64_t>(t) * kKeys;
-      const bool need_mask =
-          (k0 + kKeys > p.skv) || (p.causal && p.k_base + p.k_stride * (k0 + kKeys - 1) > q_first);
-      if (need_mask) {
-        const int64_t lim_local = lim - k0;
+        if (lane == 0) ptx::mbar_arrive(b.p_half + 8 * x);
+        // keys 64..127
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (c * 32 + e >= lim_local) sr[c][e] = __float_as_uint(-INFINITY);
-      }
-      // row maximum: eight independent 3-input max chains, then a small tree
-      float am[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) am[k] = fmaxf(__uint_as_float(sr[0][2 * k]), __uint_as_float(sr[0][2 * k + 1]));
-#pragma unroll
-      for (int i = 16; i < 128; i += 16)
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          am[k] = ptx::max3(am[k], __uint_as_float(sr[i >> 5][(i + 2 * k) & 31]),
-                            __uint_as_float(sr[i >> 5][(i + 2 * k + 1) & 31]));
-      const float mx = ptx::max3(ptx::max3(am[0], am[1], am[2]), ptx::max3(am[3], am[4], am[5]),
-                                 fmaxf(am[6], am[7]));
-      const float m_tile = mx * sl2;  // -inf stays -inf
-      bool rescale = false;
-      float factor = 1.0f;
-      if (m_ref == -INFINITY) {
-        m_ref = m_tile;  // first visible keys: O and l are still zero
-      } else if (m_tile > m_ref + kRescaleThreshold) {
-        rescale = true;
-        factor = ptx::ex2(m_ref - m_tile);
-        m_ref = m_tile;
-        l *= factor;
-      }
-      if (__any_sync(0xffffffffu, rescale)) {
-        if (!(ok = wait_pv())) break;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          ptx::tmem_ld32(tO + c * 32, o);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
-          ptx::tmem_st32(tO + c * 32, o);
+        for (int c = 2; c < 4; ++c) {
+          uint32_t pk[16];
+          exp_pack32(sr[c], sl2x2, negm2, pk, sum_a, sum_b);
+          ptx::tmem_st16(tS + c * 16, pk);
         }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(b.p_full + 8 * x);
+        float s0, s1, s2, s3;
+        ptx::f2_unpack(sum_a, s0, s1);
+        ptx::f2_unpack(sum_b, s2, s3);
+        l += (s0 + s1) + (s2 + s3);
       }
-      const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
-      const uint64_t negm2 = ptx::f2_pack(-m_use, -m_use);
-      uint64_t sum_a = ptx::f2_pack(0.0f, 0.0f), sum_b = sum_a;
-      // keys 0..63: P released early so the PV product can start on them
-      uint32_t pk0[16], pk1[16];
-      exp_pack32(sr[0], sl2x2, negm2, pk0, sum_a, sum_b);
-      exp_pack32(sr[1], sl2x2, negm2, pk1, sum_a, sum_b);
-      if (!(ok = wait_pv())) break;
-      ptx::tmem_st16(tP, pk0);
-      ptx::tmem_st16(tP + 16, pk1);
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(b.p_half + 8 * x);
-      // keys 64..127
-#pragma unroll
-      for (int c = 2; c < 4; ++c) {
-        uint32_t pk[16];
-        exp_pack32(sr[c], sl2x2, negm2, pk, sum_a, sum_b);
-        ptx::tmem_st16(tP + c * 16, pk);
-      }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(b.p_full + 8 * x);
-      float s0, s1, s2, s3;
-      ptx::f2_unpack(sum_a, s0, s1);
-      ptx::f2_unpack(sum_b, s2, s3);
-      l += (s0 + s1) + (s2 + s3);
-    }
 
-    // ---------------------------------------------------------------- epilogue
-    if (ok && n_tiles > 0) ok = wait_warp(b.o_final + 8 * x, 0, ctl, kSiteOFinal);
-    // every warp of the warpgroup arrives here exactly once; the epilogue's own barrier below
-    // is entered only if all four warps finished their loop and saw the final O
-    ok = ptx::named_bar_and(1 + x, 128, ok);
-    if (ok) {
-      if (n_tiles > 0) ptx::tc_fence_after();
-      // O / l staged in shared memory in the 128-byte-swizzled box layout of the output map,
-      // then written by TMA (whole 128-byte lines; rows past sq are clipped by the map).  Tile A
-      // stages in the K ring, tile B in the V ring: once o_final of a tile has fired, every QK
-      // (for A) or every MMA (for B) has completed, so those rings are idle.
+      // -------------------------------------------------------------- epilogue of the unit
+      if (ok && w.n_tiles > 0)
+        ok = wait_warp(b.o_final + 8 * x, static_cast<uint32_t>(kq & 1), ctl, kSiteOFinal);
+      // every warp of the warpgroup arrives here exactly once per unit; the staging barriers
+      // below are entered only if all four warps finished the unit and saw its final O
+      if (!(ok = ptx::named_bar_and(1 + x, 128, ok))) break;
+      // O into registers, then tensor memory goes back to the MMA warp for the next unit
+      uint32_t o[D / 32][32];
+      if (w.n_tiles > 0) {
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) ptx::tmem_ld32(tO + c * 32, o[c]);
+        ptx::tmem_wait_ld();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(b.o_empty + 8 * x);
+      } else {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[c][e] = 0u;
+      }
       const bool has = (m_ref != -INFINITY) && (l > 0.0f);
       const float inv = has ? 1.0f / l : 0.0f;
-      const uint32_t stage = x == 0 ? sK : sV;
-      const uint32_t row_base = stage + static_cast<uint32_t>(r) * 128u;
-      const uint32_t sw = static_cast<uint32_t>(r & 7);
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        if (n_tiles > 0) {
-          ptx::tmem_ld32(tO + c * 32, o);
-          ptx::tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0u;
-        }
+      const int boxes = p.o_bf16 ? L::kBoxesBf16 : L::kBoxesF32;
+      for (int c = 0; c < boxes; ++c) {
+        // the staging box is reusable once the previous bulk store has finished reading it
+        if (staged && store_leader) ptx::bulk_wait_read_all();
+        ptx::named_bar_sync(1 + x, 128);
         if (p.o_bf16) {
-          // box = 64 bf16 columns; columns [32c, 32c+32) are 16-byte chunks 4(c&1) .. 4(c&1)+3
-          const uint32_t box = stage + static_cast<uint32_t>(c >> 1) * 16384u;
+          // box = 64 bf16 columns = O chunks 2c, 2c+1; 16-byte chunk q holds columns 8q..8q+7
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const uint32_t chunk = static_cast<uint32_t>((c & 1) * 4 + q4);
-            const uint32_t a = box + static_cast<uint32_t>(r) * 128u + ((chunk ^ sw) << 4);
-            const uint32_t w0 = ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 0]) * inv, __uint_as_float(o[8 * q4 + 1]) * inv);
-            const uint32_t w1 = ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv, __uint_as_float(o[8 * q4 + 3]) * inv);
-            const uint32_t w2 = ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv, __uint_as_float(o[8 * q4 + 5]) * inv);
-            const uint32_t w3 = ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv, __uint_as_float(o[8 * q4 + 7]) * inv);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w0), "r"(w1), "r"(w2), "r"(w3) : "memory");
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t* src = &o[0][0] + (2 * c) * 32 + 8 * q;
+            const uint32_t a = row_addr + ((static_cast<uint32_t>(q) ^ sw) << 4);
+            const uint32_t w0 = ptx::pack_bf16x2(__uint_as_float(src[0]) * inv, __uint_as_float(src[1]) * inv);
+            const uint32_t w1 = ptx::pack_bf16x2(__uint_as_float(src[2]) * inv, __uint_as_float(src[3]) * inv);
+            const uint32_t w2 = ptx::pack_bf16x2(__uint_as_float(src[4]) * inv, __uint_as_float(src[5]) * inv);
+            const uint32_t w3 = ptx::pack_bf16x2(__uint_as_float(src[6]) * inv, __uint_as_float(src[7]) * inv);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w0), "r"(w1), "r"(w2), "r"(w3)
+                         : "memory");
           }
         } else {
-          // box = 32 fp32 columns = 8 chunks of 16 bytes
-          const uint32_t box = row_base + static_cast<uint32_t>(c) * 16384u;
+          // box = 32 fp32 columns = O chunk c; 16-byte chunk q holds columns 4q..4q+3
 #pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {
-            const uint32_t a = box + ((static_cast<uint32_t>(q4) ^ sw) << 4);
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t* src = &o[0][0] + c * 32 + 4 * q;
+            const uint32_t a = row_addr + ((static_cast<uint32_t>(q) ^ sw) << 4);
             asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a),
-                         "f"(__uint_as_float(o[4 * q4 + 0]) * inv), "f"(__uint_as_float(o[4 * q4 + 1]) * inv),
-                         "f"(__uint_as_float(o[4 * q4 + 2]) * inv), "f"(__uint_as_float(o[4 * q4 + 3]) * inv)
+                         "f"(__uint_as_float(src[0]) * inv), "f"(__uint_as_float(src[1]) * inv),
+                         "f"(__uint_as_float(src[2]) * inv), "f"(__uint_as_float(src[3]) * inv)
                          : "memory");
           }
         }
-      }
-      ptx::fence_proxy_async_smem();
-      ptx::named_bar_sync(1 + x, 128);
-      if (wq == 0 && lane == 0) {
-        const int boxes = p.o_bf16 ? (D / 64) : (D / 32);
-        const int box_cols = p.o_bf16 ? 64 : 32;
-        for (int c = 0; c < boxes; ++c)
-          ptx::tma_store_2d(&tm_o, stage + c * 16384u, h * D + c * box_cols, static_cast<int32_t>(tile_row0));
-        ptx::bulk_commit();
+        ptx::fence_proxy_async_smem();
+        ptx::named_bar_sync(1 + x, 128);
+        if (store_leader) {
+          const int box_cols = p.o_bf16 ? 64 : 32;
+          ptx::tma_store_2d(&tm_o, stage, w.h * D + c * box_cols, static_cast<int32_t>(tile_row0));
+          ptx::bulk_commit();
+        }
+        staged = true;
       }
       if (grow < p.sq)
-        p.lse[grow * p.hq + h] = has ? (m_ref * 0.69314718055994531f + logf(l)) : -INFINITY;
-      if (wq == 0 && lane == 0) ptx::bulk_wait_all();
+        p.lse[grow * p.hq + w.h] = has ? (m_ref * 0.69314718055994531f + logf(l)) : -INFINITY;
+      g += w.n_tiles;
+      if (w.n_tiles > 0) kq += 1;
     }
+    if (store_leader) ptx::bulk_wait_all();  // the last bulk stores must complete
   }
 
   ptx::tc_fence_before();
@@ -731,7 +725,7 @@ cp_status launch_tc(const TcParams& p, const CUtensorMap& mq, const CUtensorMap&
 
 }  // namespace
 
-cp_status launch_partial_attn_tc(const cp_attn_desc& d, float scale, int64_t timeout_ns, int /*num_sms*/,
+cp_status launch_partial_attn_tc(const cp_attn_desc& d, float scale, int64_t timeout_ns, int num_sms,
                                  cudaStream_t s) {
   if (d.skv == 0) {
     const int64_t n = d.sq * d.hq * d.d;
@@ -769,11 +763,9 @@ cp_status launch_partial_attn_tc(const cp_attn_desc& d, float scale, int64_t tim
     set_error("cuTensorMapEncodeTiled failed (or the driver entry point is unavailable)");
     return CP_ERR_CUDA;
   }
-  const int64_t grid = static_cast<int64_t>(p.n_pairs) * d.hq;
-  if (grid > 0x7fffffff) {
-    set_error("partial attention grid too large");
-    return CP_ERR_INVALID_ARG;
-  }
+  p.n_units = static_cast<int64_t>(p.n_pairs) * d.hq;
+  // persistent: one CTA per SM (shared memory use keeps it at one), never more CTAs than units
+  const int64_t grid = p.n_units < num_sms ? p.n_units : num_sms;
   if (d.d == 64) return launch_tc<64>(p, mq, mk, mv, mo, grid, s);
   return launch_tc<128>(p, mq, mk, mv, mo, grid, s);
 }
