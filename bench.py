@@ -63,7 +63,7 @@ def _dist():
 class Step:
     """Inputs resident on the device plus the launch sequence of one step."""
 
-    def __init__(self, cfg, device, query_rank=None, layout=None, host_copy=False):
+    def __init__(self, cfg, device, query_rank=None, layout=None, host_copy=False, fused=False):
         import context_blockwise_attention_gb300 as cpa
         from context_blockwise_attention_gb300 import workloads as wl
         self.cpa, self.wl = cpa, wl
@@ -71,6 +71,8 @@ class Step:
         self.cfg = cfg
         self.device = device
         self.layout = layout or w.layout
+        self.fused = fused and cfg != 4
+        self.fused_calls = []     # one chunk-list call per query rank (fused mode)
         self.flops = 0
         self.merge_bytes = 0
         self.reshard_bytes = 0
@@ -137,10 +139,19 @@ class Step:
                 self.merge_bytes += w.local_len * w.hq * 4 + fr * w.hq * w.d * 4
             out = torch.empty((w.local_len, w.hq, w.d), dtype=final_dtype, device=dev)
             lse = torch.empty((w.local_len, w.hq), dtype=torch.float32, device=dev)
-            self.merge_bytes += out.numel() * out.element_size() + lse.numel() * 4
-            self.merges.append((o_parts, l_parts, out, lse))
+            if self.fused:
+                # the chunks of this rank, in arrival order, in one launch; no partials, no merge
+                calls = [c for c, m in zip(self.attn_calls, self.call_meta) if m[0] == qr]
+                self.fused_calls.append(dict(q=q, chunks=[(c["k"], c["v"], c["kv_pos"]) for c in calls],
+                                             q_pos=qmap, causal=w.causal, o=out, lse=lse))
+            else:
+                self.merge_bytes += out.numel() * out.element_size() + lse.numel() * 4
+                self.merges.append((o_parts, l_parts, out, lse))
             self._output_tensors += [out, lse]
             self.rank_plans.append((qr, qmap, q, order))
+        if self.fused:
+            self.attn_calls = []  # the per-chunk partial buffers are not used
+            self.merge_bytes = 0
 
     def _build_ulysses(self):
         cpa, wl, w = self.cpa, self.wl, self.w
@@ -210,6 +221,9 @@ class Step:
         t1 = ev() if timers is not None else None
         for kw in self.attn_calls:
             cpa.partial_attn(**kw)
+            n += 1
+        for kw in self.fused_calls:
+            cpa.partial_attn_chunks(**kw)
             n += 1
         t2 = ev() if timers is not None else None
         for o_parts, l_parts, out, lse in self.merges:
@@ -428,7 +442,7 @@ def run_gpu(args):
     qr = None
     if w.query_rank >= 0:
         qr = (w.cp - 1 - rank) % w.cp
-    step = Step(args.config, dev, query_rank=qr, layout=layout, host_copy=True)
+    step = Step(args.config, dev, query_rank=qr, layout=layout, host_copy=True, fused=args.fused)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def barrier():
@@ -498,7 +512,7 @@ def run_gpu(args):
     e2e_value = world * step.flops / (e2e_total / args.steps * 1e-3) / 1e12
 
     peaks = _peaks()
-    n_attn = len(step.attn_calls)
+    n_attn = len(step.attn_calls) + len(step.fused_calls)
     achieved = step.flops / (attn_ms * 1e-3) / 1e12
     traffic = _profile_traffic(os.path.join(ROOT, "context_blockwise_attention_gb300", "csrc",
                                             "attn_tc.cu"), f"cfg{args.config}")
@@ -530,7 +544,9 @@ def run_gpu(args):
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16" if w.dtype == "bf16" else "f32",
                 "data": "synthetic (seeded N(0,1) inputs; no dataset or weights)",
-                "config": _config_dict(w, layout, {"parallelism": f"replicas x{world}"}),
+                "config": _config_dict(w, layout, {"parallelism": f"replicas x{world}",
+                                                   "path": "fused chunk list" if step.fused
+                                                   else "partial per chunk + merge"}),
                 "e2e": {"value": e2e_value, "unit": "TFLOP/s",
                         "h2d_bytes_per_step": step.h2d_bytes,
                         "d2h_bytes_per_step": step.d2h_bytes,
@@ -553,9 +569,18 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--ref-rows", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fused", action="store_true",
+                    help="consume each rank's chunks in one launch (no partials, no merge)")
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="override the workload's sequence length (smaller cases for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl != "reference":
         args.warmup = 3
+    if args.seq_len is not None:
+        import dataclasses
+        from context_blockwise_attention_gb300 import workloads as wl
+        w = wl.WORKLOADS[args.config]
+        wl.WORKLOADS[args.config] = dataclasses.replace(w, seq_len=args.seq_len)
     if args.impl == "reference":
         run_reference(args)
     else:
