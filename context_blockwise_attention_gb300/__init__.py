@@ -12,6 +12,7 @@ from .api import (  # noqa: F401
     shard_layout,
     sub_chunk_map,
     partial_attn,
+    partial_attn_chunks,
     merge_partials,
     ulysses_reshard,
     library_path,
@@ -27,6 +28,7 @@ __all__ = [
     "shard_layout",
     "sub_chunk_map",
     "partial_attn",
+    "partial_attn_chunks",
     "merge_partials",
     "ulysses_reshard",
     "library_path",

@@ -19,6 +19,7 @@ CP_F32, CP_BF16 = 0, 1
 CP_FLAG_KV_DESCENDING = 0x1
 CP_FLAG_TEST_STALL = 0x100
 CP_MAX_PARTIALS = 128
+CP_MAX_CHUNKS = 64
 
 _LAYOUTS = {"contiguous": CP_LAYOUT_CONTIGUOUS, "strided": CP_LAYOUT_STRIDED,
             CP_LAYOUT_CONTIGUOUS: CP_LAYOUT_CONTIGUOUS, CP_LAYOUT_STRIDED: CP_LAYOUT_STRIDED}
@@ -46,6 +47,11 @@ class _AttnDesc(ctypes.Structure):
         ("status", ctypes.c_void_p), ("wait_timeout_ms", ctypes.c_int32),
         ("reserved", ctypes.c_int32),
     ]
+
+
+class _KvChunk(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("skv", ctypes.c_int64),
+                ("kv_pos", _PosMap)]
 
 
 @dataclass(frozen=True)
@@ -80,6 +86,8 @@ def load_library():
     lib.cp_shard_layout.argtypes = [i64, i32, i32, i32, ctypes.POINTER(_PosMap), vp, vp]
     lib.cp_partial_attn.restype = i32
     lib.cp_partial_attn.argtypes = [ctypes.POINTER(_AttnDesc), vp]
+    lib.cp_partial_attn_chunks.restype = i32
+    lib.cp_partial_attn_chunks.argtypes = [ctypes.POINTER(_AttnDesc), i32, ctypes.POINTER(_KvChunk), vp]
     lib.cp_merge_partials.restype = i32
     lib.cp_merge_partials.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), i64, i32, i32,
                                       vp, i32, vp, vp]
@@ -188,6 +196,59 @@ def partial_attn(q, k, v, q_pos: PosMap, kv_pos: PosMap, causal=True, scale=0.0,
         desc.status = status.data_ptr()
     desc.wait_timeout_ms = int(wait_timeout_ms)
     _check(lib.cp_partial_attn(ctypes.byref(desc), _stream(stream)))
+    return o, lse
+
+
+def partial_attn_chunks(q, chunks, q_pos: PosMap, causal=True, scale=0.0, o=None, lse=None,
+                        o_dtype=None, flags=0, status=None, wait_timeout_ms=0, stream=None):
+    """Attention of query shard ``q`` against KV chunks consumed in the given (arrival) order in
+    one launch, the running softmax state carried across them.
+
+    chunks: list of (k, v, kv_pos) with k, v [Skv_c, Hkv, D] CUDA tensors and kv_pos a PosMap.
+    Returns (o, lse) over the union of the chunks' keys.
+    """
+    lib = load_library()
+    _need_cuda(q, "q")
+    n = len(chunks)
+    if n < 1 or n > CP_MAX_CHUNKS:
+        raise CpError(CP_ERR_INVALID_ARG, f"between 1 and {CP_MAX_CHUNKS} chunks")
+    sq, hq, d = q.shape
+    hkv = None
+    arr = (_KvChunk * n)()
+    for i, (k, v, kv_pos) in enumerate(chunks):
+        _need_cuda(k, "k")
+        _need_cuda(v, "v")
+        if k.dim() != 3 or v.shape != k.shape or k.shape[2] != d or k.dtype != q.dtype or v.dtype != q.dtype:
+            raise CpError(CP_ERR_INVALID_ARG, "each chunk's k and v must be [Skv, Hkv, D] in q's dtype")
+        if hkv is None:
+            hkv = k.shape[1]
+        elif k.shape[1] != hkv:
+            raise CpError(CP_ERR_INVALID_ARG, "all chunks must have the same KV head count")
+        arr[i].k, arr[i].v, arr[i].skv = k.data_ptr(), v.data_ptr(), k.shape[0]
+        arr[i].kv_pos = _PosMap(kv_pos.base, kv_pos.stride)
+    if o is None:
+        o = torch.empty((sq, hq, d), dtype=o_dtype or torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((sq, hq), dtype=torch.float32, device=q.device)
+    _need_cuda(o, "o")
+    _need_cuda(lse, "lse")
+    if tuple(o.shape) != (sq, hq, d) or tuple(lse.shape) != (sq, hq) or lse.dtype != torch.float32:
+        raise CpError(CP_ERR_INVALID_ARG, "o must be [Sq, Hq, D]; lse fp32 [Sq, Hq]")
+    desc = _AttnDesc()
+    desc.q = q.data_ptr()
+    desc.in_dtype = _dtype_code(q.dtype)
+    desc.o_dtype = _dtype_code(o.dtype)
+    desc.o, desc.lse = o.data_ptr(), lse.data_ptr()
+    desc.sq, desc.hq, desc.hkv, desc.d = sq, hq, hkv, d
+    desc.causal = 1 if causal else 0
+    desc.scale = float(scale)
+    desc.flags = int(flags)
+    desc.q_pos = _PosMap(q_pos.base, q_pos.stride)
+    if status is not None:
+        _need_cuda(status, "status")
+        desc.status = status.data_ptr()
+    desc.wait_timeout_ms = int(wait_timeout_ms)
+    _check(lib.cp_partial_attn_chunks(ctypes.byref(desc), n, arr, _stream(stream)))
     return o, lse
 
 

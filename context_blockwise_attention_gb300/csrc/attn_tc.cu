@@ -37,6 +37,7 @@
 //     CP_ERR_TIMEOUT in the caller's status word, every role leaves its loops, outstanding TMA
 //     loads, MMAs and bulk stores are drained and tensor memory is freed before the CTA exits.
 #include <math.h>
+#include <string.h>
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -71,14 +72,27 @@ struct TcParams {
   void* o;
   float* lse;
   int32_t* status;
-  int64_t sq, skv;
+  int64_t sq;
   int32_t hq, hkv, group;
   int32_t n_pairs;
   int64_t n_units;  // n_pairs * hq
   int32_t causal, o_bf16, descending, test_stall;
   float scale_log2;
-  int64_t q_base, q_stride, k_base, k_stride;
+  int64_t q_base, q_stride;
   int64_t timeout_ns;
+};
+
+// The KV chunks of one launch, in arrival order: TMA maps of K and V ([skv, hkv*d] bf16) and
+// the affine global positions.  A unit's KV tiles are the visible tiles of chunk 0, then of
+// chunk 1, ...; the online-softmax state runs across all of them.
+template <int MAXC>
+struct ChunkTable {
+  CUtensorMap k[MAXC];
+  CUtensorMap v[MAXC];
+  int64_t skv[MAXC];
+  int64_t base[MAXC];
+  int64_t stride[MAXC];
+  int32_t n;
 };
 
 template <int D>
@@ -104,9 +118,14 @@ struct Layout {
 static_assert(Layout<128>::kSmemLaunch <= 232448, "shared memory budget (D=128)");
 
 // Register split (setmaxnreg): the TMA/MMA warpgroup gives registers to the two softmax
-// warpgroups.  4 warps x 88 + 8 warps x 208 = 12 warps x 168, the launch's allocation.
-constexpr uint32_t kRegsControl = 88;
-constexpr uint32_t kRegsSoftmax = 208;
+// warpgroups.  4 warps x 120 + 8 warps x 192 = 12 warps x 168, the launch's allocation (measured
+// best of the splits without spills: the chunk loops of the TMA/MMA warps need > 104).
+#ifndef CP_REGS_CONTROL
+#define CP_REGS_CONTROL 120
+#define CP_REGS_SOFTMAX 192
+#endif
+constexpr uint32_t kRegsControl = CP_REGS_CONTROL;
+constexpr uint32_t kRegsSoftmax = CP_REGS_SOFTMAX;
 static_assert(4 * kRegsControl + 8 * kRegsSoftmax == 12 * 168, "register split must match launch");
 
 struct Bars {
@@ -158,12 +177,17 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, int64_
   }
 }
 
-__device__ __forceinline__ int64_t visible_keys(const TcParams& p, int64_t row) {
-  // keys j with k_base + k_stride * j <= q_pos(row), clipped to the chunk
+// Keys of chunk c that query `row` may see: all of them when not causal, else the keys j with
+// base + stride * j <= q_pos(row) (positions grow with the index, so they are a prefix).
+template <int MAXC>
+__device__ __forceinline__ int64_t visible_keys(const TcParams& p, const ChunkTable<MAXC>& ch, int c,
+                                                int64_t row) {
+  const int64_t skv = ch.skv[c];
+  if (!p.causal) return skv;
   const int64_t qp = p.q_base + p.q_stride * row;
-  if (qp < p.k_base) return 0;
-  const int64_t n = (qp - p.k_base) / p.k_stride + 1;
-  return n < p.skv ? n : p.skv;
+  if (qp < ch.base[c]) return 0;
+  const int64_t n = (qp - ch.base[c]) / ch.stride[c] + 1;
+  return n < skv ? n : skv;
 }
 
 // The k-th unit of CTA b: rounds of `grid` units, forward on even rounds, backward on odd ones.
@@ -172,25 +196,31 @@ __device__ __forceinline__ int64_t unit_of(int64_t k, int64_t b, int64_t grid) {
 }
 
 struct Unit {
-  int64_t row0;  // first query row of tile A
+  int64_t row0;   // first query row of tile A
+  int64_t last;   // last query row of the unit that exists
   int h, kvh;
-  int n_tiles;
+  int n_tiles;    // KV tiles over all chunks
 };
 
+// KV tiles of chunk c the unit has to visit: those holding a key visible to its last row.
+template <int MAXC>
+__device__ __forceinline__ int chunk_tiles(const TcParams& p, const ChunkTable<MAXC>& ch, int c,
+                                           const Unit& w) {
+  return static_cast<int>((visible_keys(p, ch, c, w.last) + kKeys - 1) / kKeys);
+}
+
 // Units are numbered longest first: pairs in decreasing order when causal, heads innermost.
-__device__ __forceinline__ Unit decode_unit(const TcParams& p, int64_t u) {
+template <int MAXC>
+__device__ __forceinline__ Unit decode_unit(const TcParams& p, const ChunkTable<MAXC>& ch, int64_t u) {
   Unit w;
   const int64_t pair = p.causal ? (p.n_pairs - 1 - u / p.hq) : (u / p.hq);
   w.h = static_cast<int>(u % p.hq);
   w.kvh = w.h / p.group;
   w.row0 = pair * (2 * kRows);
-  int64_t n_keys = p.skv;
-  if (p.causal) {
-    int64_t last = w.row0 + 2 * kRows - 1;
-    if (last > p.sq - 1) last = p.sq - 1;
-    n_keys = visible_keys(p, last);
-  }
-  w.n_tiles = static_cast<int>((n_keys + kKeys - 1) / kKeys);
+  w.last = w.row0 + 2 * kRows - 1;
+  if (w.last > p.sq - 1) w.last = p.sq - 1;
+  w.n_tiles = 0;
+  for (int c = 0; c < ch.n; ++c) w.n_tiles += chunk_tiles(p, ch, c, w);
   return w;
 }
 
@@ -216,11 +246,10 @@ __device__ __forceinline__ void exp_pack32(const uint32_t (&s)[32], uint64_t sl2
   }
 }
 
-template <int D>
+template <int D, int MAXC>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap tm_q,
-                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                   const __grid_constant__ CUtensorMap tm_o) {
+                   const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ ChunkTable<MAXC> ch) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -290,8 +319,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool leader = ptx::elect_one();
       if (leader) {
         ptx::tma_prefetch_desc(&tm_q);
-        ptx::tma_prefetch_desc(&tm_k);
-        ptx::tma_prefetch_desc(&tm_v);
+        for (int c = 0; c < ch.n; ++c) {
+          ptx::tma_prefetch_desc(&ch.k[c]);
+          ptx::tma_prefetch_desc(&ch.v[c]);
+        }
       }
       int64_t g = 0;        // global KV-tile counter (ring stage / phase)
       int64_t kq = 0;       // units with work seen so far (Q buffer phase)
@@ -300,19 +331,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t k = 0; ok; ++k) {
         const int64_t u = unit_of(k, cta, grid);
         if (u >= p.n_units) break;
-        const Unit w = decode_unit(p, u);
+        const Unit w = decode_unit(p, ch, u);
         if (w.n_tiles == 0) continue;
-        for (int j = 0; ok && j < w.n_tiles; ++j) {
-          const int t = p.descending ? w.n_tiles - 1 - j : j;
-          const int64_t gj = g + j;
-          const int st = static_cast<int>(gj % L::kStages);
-          const uint32_t ph = static_cast<uint32_t>((gj / L::kStages) & 1);
-          if (!(ok = wait_warp(b.k_empty + 8 * st, ph ^ 1, ctl, kSiteKEmpty))) break;
-          if (leader) {
-            ptx::mbar_arrive_expect_tx(b.k_full + 8 * st, L::kTileBytes);
-            for (int c = 0; c < L::kChunks; ++c)
-              ptx::tma_load_2d(sK + st * L::kTileBytes + c * L::kChunkBytes, &tm_k, w.kvh * D + c * 64,
-                               t * kKeys, b.k_full + 8 * st);
+        int j = 0;  // tile index within the unit, over all chunks
+        for (int c = 0; ok && c < ch.n; ++c) {
+          const int nt = chunk_tiles(p, ch, c, w);
+          for (int ti = 0; ok && ti < nt; ++ti, ++j) {
+            const int t = p.descending ? nt - 1 - ti : ti;
+            const int64_t gj = g + j;
+            const int st = static_cast<int>(gj % L::kStages);
+            const uint32_t ph = static_cast<uint32_t>((gj / L::kStages) & 1);
+            if (!(ok = wait_warp(b.k_empty + 8 * st, ph ^ 1, ctl, kSiteKEmpty))) break;
+            if (leader) {
+              ptx::mbar_arrive_expect_tx(b.k_full + 8 * st, L::kTileBytes);
+              for (int cc = 0; cc < L::kChunks; ++cc)
+                ptx::tma_load_2d(sK + st * L::kTileBytes + cc * L::kChunkBytes, &ch.k[c], w.kvh * D + cc * 64,
+                                 t * kKeys, b.k_full + 8 * st);
           }
           __syncwarp();
           kl = gj + 1;
@@ -323,8 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (leader) {
               ptx::mbar_arrive_expect_tx(b.q_full, 2 * L::kTileBytes);
               for (int x = 0; x < 2; ++x)
-                for (int c = 0; c < L::kChunks; ++c)
-                  ptx::tma_load_2d(sQ + x * L::kTileBytes + c * L::kChunkBytes, &tm_q, w.h * D + c * 64,
+                for (int cc = 0; cc < L::kChunks; ++cc)
+                  ptx::tma_load_2d(sQ + x * L::kTileBytes + cc * L::kChunkBytes, &tm_q, w.h * D + cc * 64,
                                    static_cast<int32_t>(w.row0 + x * kRows), b.q_full);
             }
             __syncwarp();
@@ -333,12 +367,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = wait_warp(b.v_empty + 8 * st, ph ^ 1, ctl, kSiteVEmpty))) break;
           if (leader) {
             ptx::mbar_arrive_expect_tx(b.v_full + 8 * st, L::kTileBytes);
-            for (int c = 0; c < L::kChunks; ++c)
-              ptx::tma_load_2d(sV + st * L::kTileBytes + c * L::kChunkBytes, &tm_v, w.kvh * D + c * 64,
+            for (int cc = 0; cc < L::kChunks; ++cc)
+              ptx::tma_load_2d(sV + st * L::kTileBytes + cc * L::kChunkBytes, &ch.v[c], w.kvh * D + cc * 64,
                                t * kKeys, b.v_full + 8 * st);
           }
           __syncwarp();
           vl = gj + 1;
+          }
         }
         g += w.n_tiles;
         kq += 1;
@@ -409,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t k = 0; ok; ++k) {
         const int64_t u = unit_of(k, cta, grid);
         if (u >= p.n_units) break;
-        const Unit w = decode_unit(p, u);
+        const Unit w = decode_unit(p, ch, u);
         if (w.n_tiles == 0) continue;
         if (!(ok = wait_warp(b.q_full, static_cast<uint32_t>(kq & 1), ctl, kSiteQ))) break;
         const int n = w.n_tiles;
@@ -489,98 +524,101 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t k = 0;; ++k) {
       const int64_t u = unit_of(k, cta, grid);
       if (u >= p.n_units) break;
-      const Unit w = decode_unit(p, u);
+      const Unit w = decode_unit(p, ch, u);
       const int64_t tile_row0 = w.row0 + x * kRows;
       const int64_t grow = tile_row0 + r;
-      const int64_t lim = p.causal ? visible_keys(p, grow) : p.skv;
-      const int64_t q_first = p.q_base + p.q_stride * tile_row0;
       float m_ref = -INFINITY;  // running maximum (log2 units of scaled scores)
       float l = 0.0f;           // running sum of 2^(x - m_ref)
 
-      for (int j = 0; j < w.n_tiles; ++j) {
-        const int t = p.descending ? w.n_tiles - 1 - j : j;
-        const int64_t gj = g + j;
-        if (!(ok = wait_warp(b.s_full + 8 * x, static_cast<uint32_t>(gj & 1), ctl, kSiteSFull))) break;
-        ptx::tc_fence_after();
-        uint32_t sr[4][32];
+      int j = 0;  // tile index within the unit, over all chunks
+      for (int ci = 0; ok && ci < ch.n; ++ci) {
+        const int nt = chunk_tiles(p, ch, ci, w);
+        // keys of this chunk visible to my row, and the leading tiles every row of my tile sees
+        // completely (keys visible to the tile's first row, whole tiles only): no mask there
+        const int lim = static_cast<int>(visible_keys(p, ch, ci, grow));
+        const int nomask = static_cast<int>(visible_keys(p, ch, ci, tile_row0) / kKeys);
+        for (int ti = 0; ti < nt; ++ti, ++j) {
+          const int t = p.descending ? nt - 1 - ti : ti;
+          const int64_t gj = g + j;
+          if (!(ok = wait_warp(b.s_full + 8 * x, static_cast<uint32_t>(gj & 1), ctl, kSiteSFull))) break;
+          ptx::tc_fence_after();
+          uint32_t sr[4][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + c * 32, sr[c]);
-        ptx::tmem_wait_ld();
+          for (int cc = 0; cc < 4; ++cc) ptx::tmem_ld32(tS + cc * 32, sr[cc]);
+          ptx::tmem_wait_ld();
 
-        const int64_t k0 = static_cast<int64_t>(t) * kKeys;
-        const bool need_mask =
-            (k0 + kKeys > p.skv) || (p.causal && p.k_base + p.k_stride * (k0 + kKeys - 1) > q_first);
-        if (need_mask) {
-          const int64_t lim_local = lim - k0;
+          if (t >= nomask) {
+            const int lim_local = lim - t * kKeys;
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (c * 32 + e >= lim_local) sr[c][e] = __float_as_uint(-INFINITY);
-        }
-        // row maximum: eight independent 3-input max chains, then a small tree
-        float am[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) am[q] = fmaxf(__uint_as_float(sr[0][2 * q]), __uint_as_float(sr[0][2 * q + 1]));
-#pragma unroll
-        for (int i = 16; i < 128; i += 16)
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            am[q] = ptx::max3(am[q], __uint_as_float(sr[i >> 5][(i + 2 * q) & 31]),
-                              __uint_as_float(sr[i >> 5][(i + 2 * q + 1) & 31]));
-        const float mx = ptx::max3(ptx::max3(am[0], am[1], am[2]), ptx::max3(am[3], am[4], am[5]),
-                                   fmaxf(am[6], am[7]));
-        const float m_tile = mx * sl2;  // -inf stays -inf
-        bool rescale = false;
-        float factor = 1.0f;
-        if (m_ref == -INFINITY) {
-          m_ref = m_tile;  // first visible keys: O and l are still zero
-        } else if (m_tile > m_ref + kRescaleThreshold) {
-          rescale = true;
-          factor = ptx::ex2(m_ref - m_tile);
-          m_ref = m_tile;
-          l *= factor;
-        }
-        if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            ptx::tmem_ld32(tO + c * 32, o);
-            ptx::tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
-            ptx::tmem_st32(tO + c * 32, o);
+              for (int e = 0; e < 32; ++e)
+                if (c * 32 + e >= lim_local) sr[c][e] = __float_as_uint(-INFINITY);
           }
-        }
-        const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
-        const uint64_t negm2 = ptx::f2_pack(-m_use, -m_use);
-        uint64_t sum_a = ptx::f2_pack(0.0f, 0.0f), sum_b = sum_a;
-        // keys 0..63: P released early so the PV product can start on them
+          // row maximum: eight independent 3-input max chains, then a small tree
+          float am[8];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t pk[16];
-          exp_pack32(sr[c], sl2x2, negm2, pk, sum_a, sum_b);
-          ptx::tmem_st16(tS + c * 16, pk);
-        }
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(b.p_half + 8 * x);
-        // keys 64..127
+          for (int q = 0; q < 8; ++q) am[q] = fmaxf(__uint_as_float(sr[0][2 * q]), __uint_as_float(sr[0][2 * q + 1]));
 #pragma unroll
-        for (int c = 2; c < 4; ++c) {
-          uint32_t pk[16];
-          exp_pack32(sr[c], sl2x2, negm2, pk, sum_a, sum_b);
-          ptx::tmem_st16(tS + c * 16, pk);
+          for (int i = 16; i < 128; i += 16)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              am[q] = ptx::max3(am[q], __uint_as_float(sr[i >> 5][(i + 2 * q) & 31]),
+                                __uint_as_float(sr[i >> 5][(i + 2 * q + 1) & 31]));
+          const float mx = ptx::max3(ptx::max3(am[0], am[1], am[2]), ptx::max3(am[3], am[4], am[5]),
+                                     fmaxf(am[6], am[7]));
+          const float m_tile = mx * sl2;  // -inf stays -inf
+          bool rescale = false;
+          float factor = 1.0f;
+          if (m_ref == -INFINITY) {
+            m_ref = m_tile;  // first visible keys: O and l are still zero
+          } else if (m_tile > m_ref + kRescaleThreshold) {
+            rescale = true;
+            factor = ptx::ex2(m_ref - m_tile);
+            m_ref = m_tile;
+            l *= factor;
+          }
+          if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              ptx::tmem_ld32(tO + c * 32, o);
+              ptx::tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
+              ptx::tmem_st32(tO + c * 32, o);
+            }
+          }
+          const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
+          const uint64_t negm2 = ptx::f2_pack(-m_use, -m_use);
+          uint64_t sum_a = ptx::f2_pack(0.0f, 0.0f), sum_b = sum_a;
+          // keys 0..63: P released early so the PV product can start on them
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t pk[16];
+            exp_pack32(sr[c], sl2x2, negm2, pk, sum_a, sum_b);
+            ptx::tmem_st16(tS + c * 16, pk);
+          }
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(b.p_half + 8 * x);
+          // keys 64..127
+#pragma unroll
+          for (int c = 2; c < 4; ++c) {
+            uint32_t pk[16];
+            exp_pack32(sr[c], sl2x2, negm2, pk, sum_a, sum_b);
+            ptx::tmem_st16(tS + c * 16, pk);
+          }
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(b.p_full + 8 * x);
+          float s0, s1, s2, s3;
+          ptx::f2_unpack(sum_a, s0, s1);
+          ptx::f2_unpack(sum_b, s2, s3);
+          l += (s0 + s1) + (s2 + s3);
         }
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(b.p_full + 8 * x);
-        float s0, s1, s2, s3;
-        ptx::f2_unpack(sum_a, s0, s1);
-        ptx::f2_unpack(sum_b, s2, s3);
-        l += (s0 + s1) + (s2 + s3);
       }
 
       // -------------------------------------------------------------- epilogue of the unit
@@ -662,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// O = 0, LSE = -inf for every row (a chunk with no keys).
+// O = 0, LSE = -inf for every row (no chunk holds a key).
 __global__ void fill_empty_kernel(void* o, int o_bf16, float* lse, int64_t rows, int64_t row_elems) {
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t n = rows * row_elems;
@@ -712,36 +750,60 @@ bool make_map(CUtensorMap* m, const void* base, int64_t tokens, int64_t row_elem
   return r == CUDA_SUCCESS;
 }
 
-template <int D>
-cp_status launch_tc(const TcParams& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                    const CUtensorMap& mo, int64_t grid, cudaStream_t s) {
+template <int D, int MAXC>
+cp_status launch_tc(const TcParams& p, const CUtensorMap& mq, const CUtensorMap& mo, const cp_attn_desc& d,
+                    const cp_kv_chunk* chunks, int n, int64_t grid, cudaStream_t s) {
+  ChunkTable<MAXC> ch;
+  memset(&ch, 0, sizeof(ch));
+  ch.n = n;
+  for (int c = 0; c < n; ++c) {
+    if (!make_map(&ch.k[c], chunks[c].k, chunks[c].skv, int64_t(d.hkv) * d.d) ||
+        !make_map(&ch.v[c], chunks[c].v, chunks[c].skv, int64_t(d.hkv) * d.d)) {
+      set_error("cuTensorMapEncodeTiled failed for chunk %d (or the driver entry point is unavailable)", c);
+      return CP_ERR_CUDA;
+    }
+    ch.skv[c] = chunks[c].skv;
+    ch.base[c] = chunks[c].kv_pos.base;
+    ch.stride[c] = chunks[c].kv_pos.stride;
+  }
   constexpr int smem = Layout<D>::kSmemLaunch;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(attn_tc_kernel<D, MAXC>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attn_tc_kernel)");
-  attn_tc_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p, mq, mk, mv, mo);
+  attn_tc_kernel<D, MAXC><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p, mq, mo, ch);
   e = cudaGetLastError();
   return e == cudaSuccess ? CP_OK : cuda_fail(e, "attn_tc_kernel launch");
 }
 
+template <int D>
+cp_status launch_tc_chunks(const TcParams& p, const CUtensorMap& mq, const CUtensorMap& mo, const cp_attn_desc& d,
+                           const cp_kv_chunk* chunks, int n, int64_t grid, cudaStream_t s) {
+  // the chunk table travels in the kernel parameters: size it to the call
+  if (n <= 1) return launch_tc<D, 1>(p, mq, mo, d, chunks, n, grid, s);
+  if (n <= 8) return launch_tc<D, 8>(p, mq, mo, d, chunks, n, grid, s);
+  return launch_tc<D, CP_MAX_CHUNKS>(p, mq, mo, d, chunks, n, grid, s);
+}
+
 }  // namespace
 
-cp_status launch_partial_attn_tc(const cp_attn_desc& d, float scale, int64_t timeout_ns, int num_sms,
-                                 cudaStream_t s) {
-  if (d.skv == 0) {
-    const int64_t n = d.sq * d.hq * d.d;
-    int64_t blocks = (n + 255) / 256;
-    if (blocks > 4096) blocks = 4096;
-    fill_empty_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(d.o, d.o_dtype == CP_BF16, d.lse,
-                                                                     d.sq * d.hq, d.d);
-    cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? CP_OK : cuda_fail(e, "fill_empty_kernel launch");
-  }
+cp_status launch_fill_empty(const cp_attn_desc& d, cudaStream_t s) {
+  const int64_t n = d.sq * d.hq * d.d;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  if (blocks < 1) blocks = 1;
+  fill_empty_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(d.o, d.o_dtype == CP_BF16, d.lse, d.sq * d.hq,
+                                                                   d.d);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? CP_OK : cuda_fail(e, "fill_empty_kernel launch");
+}
+
+cp_status launch_partial_attn_tc(const cp_attn_desc& d, const cp_kv_chunk* chunks, int n, float scale,
+                                 int64_t timeout_ns, int num_sms, cudaStream_t s) {
   TcParams p;
   p.o = d.o;
   p.lse = d.lse;
   p.status = d.status;
   p.sq = d.sq;
-  p.skv = d.skv;
   p.hq = d.hq;
   p.hkv = d.hkv;
   p.group = d.hq / d.hkv;
@@ -753,12 +815,9 @@ cp_status launch_partial_attn_tc(const cp_attn_desc& d, float scale, int64_t tim
   p.scale_log2 = scale * 1.4426950408889634f;
   p.q_base = d.q_pos.base;
   p.q_stride = d.q_pos.stride;
-  p.k_base = d.kv_pos.base;
-  p.k_stride = d.kv_pos.stride;
   p.timeout_ns = timeout_ns;
-  CUtensorMap mq, mk, mv, mo;
-  if (!make_map(&mq, d.q, d.sq, int64_t(d.hq) * d.d) || !make_map(&mk, d.k, d.skv, int64_t(d.hkv) * d.d) ||
-      !make_map(&mv, d.v, d.skv, int64_t(d.hkv) * d.d) ||
+  CUtensorMap mq, mo;
+  if (!make_map(&mq, d.q, d.sq, int64_t(d.hq) * d.d) ||
       !make_map(&mo, d.o, d.sq, int64_t(d.hq) * d.d, d.o_dtype == CP_F32)) {
     set_error("cuTensorMapEncodeTiled failed (or the driver entry point is unavailable)");
     return CP_ERR_CUDA;
@@ -766,8 +825,8 @@ cp_status launch_partial_attn_tc(const cp_attn_desc& d, float scale, int64_t tim
   p.n_units = static_cast<int64_t>(p.n_pairs) * d.hq;
   // persistent: one CTA per SM (shared memory use keeps it at one), never more CTAs than units
   const int64_t grid = p.n_units < num_sms ? p.n_units : num_sms;
-  if (d.d == 64) return launch_tc<64>(p, mq, mk, mv, mo, grid, s);
-  return launch_tc<128>(p, mq, mk, mv, mo, grid, s);
+  if (d.d == 64) return launch_tc_chunks<64>(p, mq, mo, d, chunks, n, grid, s);
+  return launch_tc_chunks<128>(p, mq, mo, d, chunks, n, grid, s);
 }
 
 }  // namespace cpattn

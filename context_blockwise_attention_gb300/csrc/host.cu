@@ -115,58 +115,97 @@ CP_API cp_status cp_shard_layout(int64_t seq_len, int32_t cp, int32_t rank, int3
   return CP_OK;
 }
 
-CP_API cp_status cp_partial_attn(const cp_attn_desc* desc, cudaStream_t stream) {
-  clear_error();
-  if (desc == nullptr) CP_INVALID("cp_partial_attn: desc is NULL");
-  const cp_attn_desc& d = *desc;
+// Checks every descriptor field except k, v, skv and kv_pos.
+static cp_status validate_desc(const cp_attn_desc& d) {
   if (d.in_dtype != CP_F32 && d.in_dtype != CP_BF16)
-    CP_INVALID("cp_partial_attn: in_dtype %d is not CP_F32 or CP_BF16", d.in_dtype);
+    CP_INVALID("partial attention: in_dtype %d is not CP_F32 or CP_BF16", d.in_dtype);
   if (d.o_dtype != CP_F32 && d.o_dtype != CP_BF16)
-    CP_INVALID("cp_partial_attn: o_dtype %d is not CP_F32 or CP_BF16", d.o_dtype);
-  if (d.sq < 0 || d.skv < 0) CP_INVALID("cp_partial_attn: negative token count");
-  if (d.sq > (int64_t(1) << 31) - 256 || d.skv > (int64_t(1) << 31) - 256)
-    CP_INVALID("cp_partial_attn: token counts must stay below 2^31");
-  if (d.hq <= 0 || d.hkv <= 0) CP_INVALID("cp_partial_attn: head counts must be positive");
-  if (d.hq % d.hkv != 0) CP_INVALID("cp_partial_attn: hq %d is not a multiple of hkv %d", d.hq, d.hkv);
-  if (d.d != 64 && d.d != 128) CP_INVALID("cp_partial_attn: head_dim %d not in {64, 128}", d.d);
-  if (d.causal != 0 && d.causal != 1) CP_INVALID("cp_partial_attn: causal must be 0 or 1");
-  if (d.q_pos.stride < 1 || d.kv_pos.stride < 1)
-    CP_INVALID("cp_partial_attn: position strides must be >= 1");
-  if (d.q_pos.base < 0 || d.kv_pos.base < 0) CP_INVALID("cp_partial_attn: positions must be >= 0");
-  // positions must stay inside int64 comfortably and inside int32 for the kernels' arithmetic
-  {
-    const double qmax = double(d.q_pos.base) + double(d.q_pos.stride) * double(d.sq);
-    const double kmax = double(d.kv_pos.base) + double(d.kv_pos.stride) * double(d.skv);
-    if (qmax > 2.0e9 || kmax > 2.0e9) CP_INVALID("cp_partial_attn: global positions exceed 2e9");
-  }
-  if (!(d.scale >= 0.0f) || isinf(d.scale)) CP_INVALID("cp_partial_attn: scale must be finite and >= 0");
+    CP_INVALID("partial attention: o_dtype %d is not CP_F32 or CP_BF16", d.o_dtype);
+  if (d.sq < 0) CP_INVALID("partial attention: negative query count");
+  if (d.sq > (int64_t(1) << 31) - 256) CP_INVALID("partial attention: token counts must stay below 2^31");
+  if (d.hq <= 0 || d.hkv <= 0) CP_INVALID("partial attention: head counts must be positive");
+  if (d.hq % d.hkv != 0) CP_INVALID("partial attention: hq %d is not a multiple of hkv %d", d.hq, d.hkv);
+  if (d.d != 64 && d.d != 128) CP_INVALID("partial attention: head_dim %d not in {64, 128}", d.d);
+  if (d.causal != 0 && d.causal != 1) CP_INVALID("partial attention: causal must be 0 or 1");
+  if (d.q_pos.stride < 1) CP_INVALID("partial attention: position strides must be >= 1");
+  if (d.q_pos.base < 0) CP_INVALID("partial attention: positions must be >= 0");
+  if (double(d.q_pos.base) + double(d.q_pos.stride) * double(d.sq) > 2.0e9)
+    CP_INVALID("partial attention: global positions exceed 2e9");
+  if (!(d.scale >= 0.0f) || isinf(d.scale)) CP_INVALID("partial attention: scale must be finite and >= 0");
   if (d.flags & ~(CP_FLAG_KV_DESCENDING | CP_FLAG_TEST_STALL))
-    CP_INVALID("cp_partial_attn: unknown flag bits 0x%x", d.flags);
-  if (d.wait_timeout_ms < 0) CP_INVALID("cp_partial_attn: wait_timeout_ms must be >= 0");
+    CP_INVALID("partial attention: unknown flag bits 0x%x", d.flags);
+  if (d.wait_timeout_ms < 0) CP_INVALID("partial attention: wait_timeout_ms must be >= 0");
   if (d.sq > 0) {
     if (d.q == nullptr || d.o == nullptr || d.lse == nullptr)
-      CP_INVALID("cp_partial_attn: q, o and lse must not be NULL");
+      CP_INVALID("partial attention: q, o and lse must not be NULL");
     if (!aligned16(d.q) || !aligned16(d.o) || (reinterpret_cast<uintptr_t>(d.lse) & 3u))
-      CP_INVALID("cp_partial_attn: q and o must be 16-byte aligned, lse 4-byte aligned");
+      CP_INVALID("partial attention: q and o must be 16-byte aligned, lse 4-byte aligned");
+    if (d.in_dtype == CP_BF16 && (int64_t(d.hq) * d.d * 2) % 16 != 0)
+      CP_INVALID("partial attention: row strides must be multiples of 16 bytes");
   }
-  if (d.skv > 0 && d.sq > 0) {
-    if (d.k == nullptr || d.v == nullptr) CP_INVALID("cp_partial_attn: k and v must not be NULL");
-    if (!aligned16(d.k) || !aligned16(d.v)) CP_INVALID("cp_partial_attn: k and v must be 16-byte aligned");
+  return CP_OK;
+}
+
+static cp_status validate_chunk(const cp_attn_desc& d, const cp_kv_chunk& c, int idx) {
+  if (c.skv < 0) CP_INVALID("partial attention: chunk %d has a negative token count", idx);
+  if (c.skv > (int64_t(1) << 31) - 256) CP_INVALID("partial attention: chunk %d token count must stay below 2^31", idx);
+  if (c.kv_pos.stride < 1) CP_INVALID("partial attention: chunk %d position stride must be >= 1", idx);
+  if (c.kv_pos.base < 0) CP_INVALID("partial attention: chunk %d positions must be >= 0", idx);
+  if (double(c.kv_pos.base) + double(c.kv_pos.stride) * double(c.skv) > 2.0e9)
+    CP_INVALID("partial attention: chunk %d global positions exceed 2e9", idx);
+  if (c.skv > 0 && d.sq > 0) {
+    if (c.k == nullptr || c.v == nullptr) CP_INVALID("partial attention: chunk %d k and v must not be NULL", idx);
+    if (!aligned16(c.k) || !aligned16(c.v)) CP_INVALID("partial attention: chunk %d k and v must be 16-byte aligned", idx);
+    if (d.in_dtype == CP_BF16 && (int64_t(d.hkv) * d.d * 2) % 16 != 0)
+      CP_INVALID("partial attention: row strides must be multiples of 16 bytes");
   }
-  if (d.in_dtype == CP_BF16 && d.skv > 0 && d.sq > 0) {
-    // tensor-map strides (row = heads * d * 2 bytes) must be multiples of 16 bytes
-    if ((int64_t(d.hq) * d.d * 2) % 16 != 0 || (int64_t(d.hkv) * d.d * 2) % 16 != 0)
-      CP_INVALID("cp_partial_attn: row strides must be multiples of 16 bytes");
-  }
+  return CP_OK;
+}
+
+// Launches the partial over the chunks that hold keys (chunks without keys contribute nothing).
+static cp_status run_partial(const cp_attn_desc& d, const cp_kv_chunk* chunks, int n, cudaStream_t stream) {
   if (d.sq == 0) return CP_OK;
   int dev = 0, sms = 0;
   cp_status st = require_sm103(&dev, &sms);
   if (st != CP_OK) return st;
+  cp_kv_chunk live[CP_MAX_CHUNKS];
+  int m = 0;
+  for (int i = 0; i < n; ++i)
+    if (chunks[i].skv > 0) live[m++] = chunks[i];
+  if (m == 0) return launch_fill_empty(d, stream);
   const float scale = d.scale > 0.0f ? d.scale : 1.0f / sqrtf(static_cast<float>(d.d));
   const int64_t timeout_ns =
       static_cast<int64_t>(d.wait_timeout_ms > 0 ? d.wait_timeout_ms : 2000) * 1000000LL;
-  if (d.in_dtype == CP_F32) return launch_partial_attn_simt(d, scale, timeout_ns, stream);
-  return launch_partial_attn_tc(d, scale, timeout_ns, sms, stream);
+  if (d.in_dtype == CP_F32) return launch_partial_attn_simt(d, live, m, scale, stream);
+  return launch_partial_attn_tc(d, live, m, scale, timeout_ns, sms, stream);
+}
+
+CP_API cp_status cp_partial_attn(const cp_attn_desc* desc, cudaStream_t stream) {
+  clear_error();
+  if (desc == nullptr) CP_INVALID("cp_partial_attn: desc is NULL");
+  cp_status st = validate_desc(*desc);
+  if (st != CP_OK) return st;
+  cp_kv_chunk c;
+  c.k = desc->k;
+  c.v = desc->v;
+  c.skv = desc->skv;
+  c.kv_pos = desc->kv_pos;
+  if ((st = validate_chunk(*desc, c, 0)) != CP_OK) return st;
+  return run_partial(*desc, &c, 1, stream);
+}
+
+CP_API cp_status cp_partial_attn_chunks(const cp_attn_desc* desc, int32_t n_chunks, const cp_kv_chunk* chunks,
+                                        cudaStream_t stream) {
+  clear_error();
+  if (desc == nullptr) CP_INVALID("cp_partial_attn_chunks: desc is NULL");
+  if (n_chunks < 1 || n_chunks > CP_MAX_CHUNKS)
+    CP_INVALID("cp_partial_attn_chunks: n_chunks=%d not in [1, %d]", n_chunks, CP_MAX_CHUNKS);
+  if (chunks == nullptr) CP_INVALID("cp_partial_attn_chunks: chunks is NULL");
+  cp_status st = validate_desc(*desc);
+  if (st != CP_OK) return st;
+  for (int i = 0; i < n_chunks; ++i)
+    if ((st = validate_chunk(*desc, chunks[i], i)) != CP_OK) return st;
+  return run_partial(*desc, chunks, n_chunks, stream);
 }
 
 CP_API cp_status cp_merge_partials(int32_t n, const float* const* o_parts,

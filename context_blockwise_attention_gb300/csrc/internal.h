@@ -24,10 +24,14 @@ cp_status cuda_fail(cudaError_t e, const char* what);
 cp_status launch_fill_positions(int32_t* out, int64_t n, int64_t base, int64_t stride,
                                 cudaStream_t s);
 
-cp_status launch_partial_attn_simt(const cp_attn_desc& d, float scale, int64_t timeout_ns,
+// Partial attention of desc's query shard against chunks[0..n) (n >= 1, chunks with skv > 0
+// only), consumed in order with the running state carried across chunks.
+cp_status launch_partial_attn_simt(const cp_attn_desc& d, const cp_kv_chunk* chunks, int n, float scale,
                                    cudaStream_t s);
-cp_status launch_partial_attn_tc(const cp_attn_desc& d, float scale, int64_t timeout_ns,
-                                 int num_sms, cudaStream_t s);
+cp_status launch_partial_attn_tc(const cp_attn_desc& d, const cp_kv_chunk* chunks, int n, float scale,
+                                 int64_t timeout_ns, int num_sms, cudaStream_t s);
+// O = 0, LSE = -inf for every row of desc's query shard (no visible key at all).
+cp_status launch_fill_empty(const cp_attn_desc& d, cudaStream_t s);
 
 struct MergeArgs {
   int32_t n;

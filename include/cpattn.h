@@ -128,6 +128,39 @@ typedef struct {
 
 cp_status cp_partial_attn(const cp_attn_desc* desc, cudaStream_t stream);
 
+/* Largest number of KV chunks one cp_partial_attn_chunks call accepts. */
+#define CP_MAX_CHUNKS 64
+
+/* One KV chunk for cp_partial_attn_chunks: device [skv, hkv, d] K and V (in_dtype of the
+ * descriptor) and the global positions of its tokens. */
+typedef struct {
+  const void* k;
+  const void* v;
+  int64_t skv;
+  cp_posmap kv_pos;
+} cp_kv_chunk;
+
+/*
+ * Attention of one query shard against a list of KV chunks, consumed in the given (arrival)
+ * order inside one launch, with the running maximum, running sum and accumulator carried from
+ * chunk to chunk.
+ *   [FCP] section 3.3: each arriving KV block updates the running max and running sum of every
+ *   local query block; the result equals attention over the union of the blocks whatever their
+ *   order.  Equivalent to one cp_partial_attn per chunk followed by cp_merge_partials, without
+ *   writing or re-reading the per-chunk partials.
+ * desc supplies q, o, lse, sq, hq, hkv, d, causal, scale, q_pos, in_dtype, o_dtype, flags,
+ * status and wait_timeout_ms exactly as for cp_partial_attn; its k, v, skv and kv_pos are
+ * ignored.  o/lse receive the (O, LSE) over the union of the chunks' keys (O = 0, LSE = -inf for
+ * rows that see no key).
+ * Arguments:
+ *   n_chunks   1 <= n_chunks <= CP_MAX_CHUNKS
+ *   chunks     host array [n_chunks], read during the call
+ * Errors: as cp_partial_attn, plus CP_ERR_INVALID_ARG for a bad chunk (null pointer with
+ * skv > 0, misaligned pointer, stride < 1, negative base or skv).
+ */
+cp_status cp_partial_attn_chunks(const cp_attn_desc* desc, int32_t n_chunks, const cp_kv_chunk* chunks,
+                                 cudaStream_t stream);
+
 /*
  * Merge n partials of the same query rows into exact attention.
  *   [PCP/DCP] sections 2.3 and 4.2 (global_softmax): global max first, then exponentials

@@ -108,6 +108,37 @@ def test_cfg5_rank7_sampled_outliers():
     _check_rank_workload(5, "strided", 128)
 
 
+def _check_fused(cfg, layout, sample):
+    w = wl.WORKLOADS[cfg]
+    step = bench.Step(cfg, DEV, layout=layout, fused=True)
+    for kw in step.fused_calls:
+        kw["o"].fill_(float("nan"))
+        kw["lse"].fill_(float("nan"))
+    step.run()
+    torch.cuda.synchronize()
+    kv_cpu = {r: (k.cpu(), v.cpu()) for r, (k, v) in step.kv.items()}
+    all_k = torch.cat([kv_cpu[r][0] for r in range(w.cp)])
+    all_v = torch.cat([kv_cpu[r][1] for r in range(w.cp)])
+    all_pos = np.concatenate([oracle.shard_positions(w.seq_len, w.cp, r, layout) for r in range(w.cp)])
+    for (qr, qmap, q, order), kw in zip(step.rank_plans, step.fused_calls):
+        qpos = oracle.shard_positions(w.seq_len, w.cp, qr, layout)
+        rows = _rows_for(w, w.local_len + qr, sample)
+        idx = torch.from_numpy(rows).to(DEV)
+        o_ref, l_ref = oracle.attention(q[idx].cpu(), all_k, all_v, qpos[rows], all_pos, causal=w.causal)
+        compare_partial(kw["o"][idx].float().cpu().numpy(), kw["lse"][idx].cpu().numpy(), o_ref, l_ref,
+                        TOL_BF16_O, TOL_BF16_LSE, f"cfg{cfg} fused rank{qr}")
+
+
+def test_cfg2_fused_full():
+    # one launch consumes the 8 chunks in arrival order; every row and head
+    _check_fused(2, "strided", None)
+
+
+def test_cfg5_fused_sampled():
+    # 64 chunks with K outliers in one launch
+    _check_fused(5, "strided", 128)
+
+
 def test_cfg4_ulysses():
     w = wl.WORKLOADS[4]
     cp, S = w.cp, w.seq_len

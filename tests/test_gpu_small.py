@@ -235,3 +235,76 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     o, l, o_ref, l_ref = _run_partial(sq, skv, hq, hkv, d, True, PosMap(0, 1), PosMap(0, 1),
                                       torch.bfloat16, seed=77)
     compare_partial(o, l, o_ref, l_ref, TOL_BF16_O, TOL_BF16_LSE, "after fault")
+
+
+# ------------------------------------------------------------------------------- fused chunk list
+
+# (sq, hq, hkv, d, causal, q map, [(skv, kv map)], dtype)
+FUSED_CASES = [
+    (384, 4, 2, 128, True, PosMap(7, 8),
+     [(256, PosMap(0, 8)), (300, PosMap(2, 8)), (0, PosMap(5, 8)), (129, PosMap(3, 8))], torch.bfloat16),
+    (300, 4, 1, 64, True, PosMap(3, 4), [(777, PosMap(0, 1)), (128, PosMap(5000, 1))], torch.bfloat16),
+    (256, 2, 2, 64, False, PosMap(0, 1), [(100, PosMap(0, 1)), (200, PosMap(100, 1)), (50, PosMap(300, 1))],
+     torch.bfloat16),
+    (513, 8, 2, 128, True, PosMap(0, 1), [(200, PosMap(300, 1)), (300, PosMap(0, 1))], torch.bfloat16),
+    (200, 4, 2, 128, True, PosMap(1, 3), [(333, PosMap(0, 1)), (64, PosMap(2, 5))], torch.float32),
+]
+
+
+def _fused_inputs(case, seed):
+    sq, hq, hkv, d, causal, qm, chunk_specs, dtype = case
+    q = wl.normal((sq, hq, d), dtype, seed, 0.5, device=DEV)
+    chunks = []
+    for i, (skv, km) in enumerate(chunk_specs):
+        k = wl.normal((skv, hkv, d), dtype, seed + 10 * i + 1, 0.5, device=DEV)
+        v = wl.normal((skv, hkv, d), dtype, seed + 10 * i + 2, 1.0, device=DEV)
+        chunks.append((k, v, km))
+    return q, chunks
+
+
+def _fused_oracle(case, q, chunks):
+    sq, hq, hkv, d, causal, qm, _, _ = case
+    k_all = torch.cat([c[0].cpu() for c in chunks])
+    v_all = torch.cat([c[1].cpu() for c in chunks])
+    pos = np.concatenate([_pos(c[2], c[0].shape[0]) for c in chunks])
+    return oracle.attention(q.cpu(), k_all, v_all, _pos(qm, sq), pos, causal=causal)
+
+
+@pytest.mark.parametrize("case", FUSED_CASES, ids=[f"fused{i}" for i in range(len(FUSED_CASES))])
+def test_fused_chunks_parity_and_order(case):
+    sq, hq, hkv, d, causal, qm, _, dtype = case
+    q, chunks = _fused_inputs(case, 31)
+    o_ref, l_ref = _fused_oracle(case, q, chunks)
+    tol_o, tol_l = (TOL_F32, TOL_F32) if dtype == torch.float32 else (TOL_BF16_O, TOL_BF16_LSE)
+    for order in (list(range(len(chunks))), list(range(len(chunks)))[::-1]):
+        o = torch.full((sq, hq, d), float("nan"), dtype=torch.float32, device=DEV)
+        lse = torch.full((sq, hq), float("nan"), device=DEV)
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        cpa.partial_attn_chunks(q, [chunks[i] for i in order], qm, causal=causal, o=o, lse=lse,
+                                status=status)
+        torch.cuda.synchronize()
+        assert status.item() == 0
+        compare_partial(o.cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, tol_o, tol_l,
+                        f"fused {case[:6]} order {order}")
+
+
+def test_fused_matches_partials_plus_merge():
+    case = FUSED_CASES[0]
+    sq, hq, hkv, d, causal, qm, _, _ = case
+    q, chunks = _fused_inputs(case, 77)
+    o_f, l_f = cpa.partial_attn_chunks(q, chunks, qm, causal=causal, o_dtype=torch.bfloat16)
+    parts = [cpa.partial_attn(q, k, v, qm, km, causal=causal) for k, v, km in chunks if k.shape[0] > 0]
+    o_m, l_m = cpa.merge_partials([p[0] for p in parts], [p[1] for p in parts], out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    fin = torch.isfinite(l_m)
+    assert torch.equal(torch.isneginf(l_f), torch.isneginf(l_m))
+    assert (o_f.float() - o_m.float()).abs().max().item() <= TOL_BF16_O
+    assert (l_f[fin] - l_m[fin]).abs().max().item() <= TOL_BF16_LSE
+
+
+def test_fused_all_chunks_empty():
+    q = wl.normal((50, 2, 64), torch.bfloat16, 1, device=DEV)
+    e = torch.empty((0, 2, 64), dtype=torch.bfloat16, device=DEV)
+    o, l = cpa.partial_attn_chunks(q, [(e, e, PosMap(0, 1)), (e, e, PosMap(9, 1))], PosMap(0, 1))
+    torch.cuda.synchronize()
+    assert torch.all(o == 0) and torch.all(torch.isneginf(l))

@@ -30,6 +30,7 @@ def test_desc_layout_matches_header():
     # the ctypes mirror must match the C struct size (pointers 8, int64 8, int32/float 4)
     assert ctypes.sizeof(api._AttnDesc) == 136
     assert ctypes.sizeof(api._PosMap) == 16
+    assert ctypes.sizeof(api._KvChunk) == 40
 
 
 def _layout(seq, cp, rank, kind):
@@ -131,3 +132,23 @@ def test_python_wrapper_rejects_cpu_tensors():
     q = torch.zeros(4, 2, 64)
     with pytest.raises(cpa.CpError):
         cpa.partial_attn(q, q, q, cpa.PosMap(0, 1), cpa.PosMap(0, 1))
+
+
+def test_partial_attn_chunks_rejects():
+    lib = cpa.load_library()
+    d = _desc()
+    ch = (api._KvChunk * 2)()
+    for c in ch:
+        c.k, c.v, c.skv, c.kv_pos = 0x1000, 0x2000, 128, api._PosMap(0, 1)
+    assert lib.cp_partial_attn_chunks(ctypes.byref(d), 0, ch, None) == api.CP_ERR_INVALID_ARG
+    assert lib.cp_partial_attn_chunks(ctypes.byref(d), 65, ch, None) == api.CP_ERR_INVALID_ARG
+    assert lib.cp_partial_attn_chunks(ctypes.byref(d), 2, None, None) == api.CP_ERR_INVALID_ARG
+    assert lib.cp_partial_attn_chunks(None, 2, ch, None) == api.CP_ERR_INVALID_ARG
+    ch[1].kv_pos = api._PosMap(0, 0)
+    assert lib.cp_partial_attn_chunks(ctypes.byref(d), 2, ch, None) == api.CP_ERR_INVALID_ARG
+    ch[1].kv_pos = api._PosMap(0, 1)
+    ch[1].k = 0
+    assert lib.cp_partial_attn_chunks(ctypes.byref(d), 2, ch, None) == api.CP_ERR_INVALID_ARG
+    ch[1].k = 0x1008
+    assert lib.cp_partial_attn_chunks(ctypes.byref(d), 2, ch, None) == api.CP_ERR_INVALID_ARG
+    assert b"chunk 1" in lib.cp_last_error()
