@@ -255,6 +255,23 @@ class Step:
 
 # ----------------------------------------------------------------------------- measurement
 
+def aggregate(total_ms_local, flops_local, steps, world, device=None):
+    """Whole-job numbers of a timed region run on every rank: the slowest rank's time and the sum
+    of all ranks' FLOPs.  Returns (ms_per_step, TFLOP/s).  With world == 1 no process group is
+    touched; otherwise the current default group (nccl or gloo) reduces on `device`."""
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([float(total_ms_local)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        f = torch.tensor([float(flops_local)], dtype=torch.float64, device=device)
+        dist.all_reduce(f, op=dist.ReduceOp.SUM)
+        total_ms_local, flops = float(t.item()), float(f.item())
+    else:
+        flops = float(flops_local)
+    ms_per_step = total_ms_local / steps
+    return ms_per_step, flops / (ms_per_step * 1e-3) / 1e12
+
+
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -472,14 +489,7 @@ def run_gpu(args):
         step_ms.append(a.elapsed_time(b))
     barrier()
     clocks = sampler.stop()
-    total_ms = sum(step_ms)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms_per_step = total_ms / args.steps
-    value = world * step.flops / (ms_per_step * 1e-3) / 1e12
+    ms_per_step, value = aggregate(sum(step_ms), step.flops, args.steps, world, dev)
 
     def seg(name):
         # total device time of one kind of launch per step (a step may record several intervals)
@@ -503,13 +513,7 @@ def run_gpu(args):
         b.record(stream)
         torch.cuda.synchronize()
         e2e_ms.append(a.elapsed_time(b))
-    e2e_total = sum(e2e_ms)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_total = float(t.item())
-    e2e_value = world * step.flops / (e2e_total / args.steps * 1e-3) / 1e12
+    e2e_ms_per_step, e2e_value = aggregate(sum(e2e_ms), step.flops, args.steps, world, dev)
 
     peaks = _peaks()
     n_attn = len(step.attn_calls) + len(step.fused_calls)
@@ -533,6 +537,32 @@ def run_gpu(args):
         extra["reshard"] = {"ms": reshard_ms, "GB/s": gbs, "frac": gbs / peaks["hbm"],
                             "bytes": step.reshard_bytes}
 
+    fused = None
+    if not args.fused and args.config != 4 and not args.no_fused:
+        # the same workload through the fused chunk-list path (f1), timed the same way
+        fstep = Step(args.config, dev, query_rank=qr, layout=layout, fused=True)
+        for _ in range(args.warmup):
+            fstep.run()
+        barrier()
+        fms, fattn = [], {"attn": [], "merge": [], "reshard": []}
+        for _ in range(args.steps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fstep.run(fattn)
+            b.record(stream)
+            torch.cuda.synchronize()
+            fms.append(a.elapsed_time(b))
+        barrier()
+        f_ms, f_value = aggregate(sum(fms), fstep.flops, args.steps, world, dev)
+        f_attn_ms = sum(s_.elapsed_time(e_) for s_, e_ in fattn["attn"]) / args.steps
+        f_ach = fstep.flops / (f_attn_ms * 1e-3) / 1e12
+        fused = {"value": f_value, "unit": "TFLOP/s", "ms_per_step": f_ms,
+                 "attn_tflops": f_ach, "attn_frac": f_ach / peaks["bf16"],
+                 "launches_per_step": len(fstep.fused_calls),
+                 "path": "one cp_partial_attn_chunks per query rank (no partials, no merge)"}
+        del fstep
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         t, fl, desc = oracle_sample(args.config, args.ref_rows)
@@ -550,9 +580,9 @@ def run_gpu(args):
                 "e2e": {"value": e2e_value, "unit": "TFLOP/s",
                         "h2d_bytes_per_step": step.h2d_bytes,
                         "d2h_bytes_per_step": step.d2h_bytes,
-                        "ms_per_step": e2e_total / args.steps},
+                        "ms_per_step": e2e_ms_per_step},
                 "gpu_launches": launches,
-                "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks, **extra}
+                "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks, "fused": fused, **extra}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -569,6 +599,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--ref-rows", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fused", action="store_true",
+                    help="skip the extra measurement of the fused chunk-list path")
     ap.add_argument("--fused", action="store_true",
                     help="consume each rank's chunks in one launch (no partials, no merge)")
     ap.add_argument("--seq-len", type=int, default=None,
