@@ -8,12 +8,19 @@ positions a rank sees stay global (same section, on position encodings).
 Strided ("zig-zag") split: "Zig-Zag Ring Attention" article, section 4.2: instead of
 consecutive blocks, GPU 0 takes tokens 0, 4, 8, ... and GPU 1 takes 1, 5, 9, ... (4 GPUs), so
 rank ``r`` holds ``r, r + cp, r + 2 cp, ...``.
+
+Two-block split: the same article (sections 4.2 and 5.2) states the aim of the zig-zag
+assignment -- every GPU gets both early and late tokens, so causal work is even.  The
+block-granular way to meet it (not printed on the pages; offered as an extra layout): cut the
+sequence into ``2 cp`` equal blocks and give rank ``r`` block ``r`` and block ``2 cp - 1 - r``,
+in that (ascending) order.
 """
 
 import numpy as np
 
 CONTIGUOUS = "contiguous"
 STRIDED = "strided"
+TWO_BLOCK = "two_block"
 
 
 def shard_positions(seq_len: int, cp: int, rank: int, kind: str) -> np.ndarray:
@@ -32,6 +39,13 @@ def shard_positions(seq_len: int, cp: int, rank: int, kind: str) -> np.ndarray:
     if kind == STRIDED:
         # every cp-th token, starting at the rank's own index
         return np.array([rank + cp * i for i in range(local_len)], dtype=np.int64)
+    if kind == TWO_BLOCK:
+        if seq_len % (2 * cp) != 0:
+            raise ValueError("the two-block split needs seq_len to be a multiple of 2 * cp")
+        block = seq_len // (2 * cp)
+        early = [rank * block + i for i in range(block)]
+        late = [(2 * cp - 1 - rank) * block + i for i in range(block)]
+        return np.array(early + late, dtype=np.int64)
     raise ValueError(f"unknown layout kind {kind!r}")
 
 

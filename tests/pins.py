@@ -253,8 +253,22 @@ def check_layouts(orc):
             got = orc.shard_positions(seq_len, cp, r, "contiguous")
             assert len(got) == local_len and got[0] == r * local_len
             assert np.all(np.diff(got) == 1)
-    for kind in ("contiguous", "strided"):
-        for seq_len, cp in ((64, 4), (48, 8), (7, 7), (32768, 8)):
+    # two-block split, written out by hand for S=16, cp=2 and S=24, cp=3
+    assert list(orc.shard_positions(16, 2, 0, "two_block")) == [0, 1, 2, 3, 12, 13, 14, 15]
+    assert list(orc.shard_positions(16, 2, 1, "two_block")) == [4, 5, 6, 7, 8, 9, 10, 11]
+    assert list(orc.shard_positions(24, 3, 1, "two_block")) == [4, 5, 6, 7, 16, 17, 18, 19]
+    # its point: every rank's causal work against the whole sequence is the same, in closed form
+    # b^2 (2cp - 1) + b (b + 1) for blocks of b = S / (2 cp) tokens
+    for seq_len, cp in ((64, 4), (48, 8), (96, 3)):
+        b = seq_len // (2 * cp)
+        for r in range(cp):
+            work = orc.visible_pair_count(orc.shard_positions(seq_len, cp, r, "two_block"),
+                                          np.arange(seq_len), True)
+            assert work == b * b * (2 * cp - 1) + b * (b + 1), "two-block split is not balanced"
+    for kind in ("contiguous", "strided", "two_block"):
+        for seq_len, cp in ((64, 4), (48, 8), (7, 7), (14, 7), (32768, 8)):
+            if kind == "two_block" and seq_len % (2 * cp):
+                continue
             allpos = np.concatenate([orc.shard_positions(seq_len, cp, r, kind) for r in range(cp)])
             assert np.array_equal(np.sort(allpos), np.arange(seq_len)), "layout is not a cover"
             # every rank's causal pairs against every chunk add up to S(S+1)/2
@@ -268,7 +282,7 @@ def check_ulysses(orc):
     (cp, hq, hkv, per_rank), = [tuple(int(x) for x in r) for r in golden_rows("ulysses_cp4.txt")]
     rng = np.random.default_rng(21)
     seq, d = 32, 4
-    for kind in ("contiguous", "strided"):
+    for kind in ("contiguous", "strided", "two_block"):
         pos = [orc.shard_positions(seq, cp, r, kind) for r in range(cp)]
         q_full = rng.standard_normal((seq, hq, d))
         k_full = rng.standard_normal((seq, hkv, d)) * 0.3

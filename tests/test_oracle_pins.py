@@ -67,6 +67,8 @@ MUTANTS = [
     ("strided_row_major", "layouts", "rank + cp * i", "rank * local_len + i"),
     ("contiguous_start", "layouts", "start = rank * local_len", "start = rank * cp"),
     ("visible_strict", "layouts", 'side="right"', 'side="left"'),
+    ("two_block_mirror", "layouts", "late = [(2 * cp - 1 - rank) * block + i",
+     "late = [(cp + rank) * block + i"),
     ("ulysses_interleaved_q_heads", "ulysses",
      "out[r][np.asarray(positions[s])] = x_shards[s][:, r * hl:(r + 1) * hl, :]",
      "out[r][np.asarray(positions[s])] = x_shards[s][:, r::cp, :]"),
