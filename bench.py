@@ -78,7 +78,10 @@ class Step:
         self.reshard_bytes = 0
         self.launches = 0
         self.attn_calls = []      # list of (kwargs) for partial_attn
-        self.call_meta = []       # (query rank, source rank, sub-chunk) of each call
+        # per partial call: (query rank, first shard row, rows, source rank, first source row, keys)
+        self.call_meta = []
+        self.rank_plans = []      # (query rank, q shard, merged out, merged lse) per query rank
+        self.fused_meta = []      # query rank of each fused call
         self.merges = []          # list of (o_parts, l_parts, o_out, l_out)
         self.host_inputs = []     # (host pinned, device) pairs copied in e2e mode
         self.host_outputs = []    # (device, host pinned) pairs read back in e2e mode
@@ -93,10 +96,23 @@ class Step:
             self.host_outputs = [(t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True))
                                  for t in self._output_tensors]
 
+    def _chunk_plan(self):
+        """KV chunks of every source rank, src-major: (src, first local row, tokens, map).  Each
+        affine segment of a shard is cut into runs of at most the workload's chunk length."""
+        cpa, w = self.cpa, self.w
+        plan = []
+        for src in range(w.cp):
+            row = 0
+            for m, n in cpa.shard_segments(w.seq_len, w.cp, src, self.layout):
+                step = min(w.chunk_len, n)
+                for sub in range(n // step):
+                    plan.append((src, row + sub * step, step, cpa.sub_chunk_map(m, sub, step)))
+                row += n
+        return plan
+
     def _build_ranks(self, ranks):
         cpa, wl, w = self.cpa, self.wl, self.w
         dev = self.device
-        dt = w.torch_dtype
         o_dtype = torch.float32
         final_dtype = torch.float32 if w.dtype == "f32" else torch.bfloat16
         kv = {}
@@ -109,48 +125,52 @@ class Step:
             kv[r] = (k, v)
             self._input_tensors += [k, v]
         self.kv = kv
-        self.rank_plans = []
+        plan = self._chunk_plan()
+        self.n_chunks = len(plan)
         for qr in ranks:
-            qmap = cpa.shard_layout(w.seq_len, w.cp, qr, self.layout)
+            # each affine segment of the query shard (one, or two for the two-block layout) is
+            # its own query block: its partials, its merge (or its fused call)
+            qsegs = cpa.shard_segments(w.seq_len, w.cp, qr, self.layout)
             q = wl.shard_tensor(w, "q", qr, device=dev)
             self._input_tensors.append(q)
             self.pos_bufs.append((qr, torch.empty(w.local_len, dtype=torch.int32, device=dev)))
-            order = wl.arrival_order(w.n_chunks, w.order_seed + 17 * qr)
-            o_parts, l_parts = [], []
-            for ci in order:
-                src, sub = divmod(int(ci), w.chunks_per_shard)
-                kmap = cpa.sub_chunk_map(cpa.shard_layout(w.seq_len, w.cp, src, self.layout), sub,
-                                         w.chunk_len)
-                n_vis = cpa.visible_pairs(qmap, w.local_len, kmap, w.chunk_len, w.causal)
-                if w.causal and n_vis == 0:
-                    continue  # chunk entirely in the future of this shard: never issued
-                k, v = kv[src]
-                ks = k[sub * w.chunk_len:(sub + 1) * w.chunk_len]
-                vs = v[sub * w.chunk_len:(sub + 1) * w.chunk_len]
-                o = torch.empty((w.local_len, w.hq, w.d), dtype=o_dtype, device=dev)
-                l = torch.empty((w.local_len, w.hq), dtype=torch.float32, device=dev)
-                self.attn_calls.append(dict(q=q, k=ks, v=vs, q_pos=qmap, kv_pos=kmap,
-                                            causal=w.causal, o=o, lse=l))
-                self.call_meta.append((qr, src, sub))
-                self.flops += 4 * w.d * w.hq * n_vis
-                o_parts.append(o)
-                l_parts.append(l)
-                fr = cpa.finite_rows(qmap, w.local_len, kmap, w.chunk_len, w.causal)
-                self.merge_bytes += w.local_len * w.hq * 4 + fr * w.hq * w.d * 4
+            order = wl.arrival_order(len(plan), w.order_seed + 17 * qr)
             out = torch.empty((w.local_len, w.hq, w.d), dtype=final_dtype, device=dev)
             lse = torch.empty((w.local_len, w.hq), dtype=torch.float32, device=dev)
-            if self.fused:
-                # the chunks of this rank, in arrival order, in one launch; no partials, no merge
-                calls = [c for c, m in zip(self.attn_calls, self.call_meta) if m[0] == qr]
-                self.fused_calls.append(dict(q=q, chunks=[(c["k"], c["v"], c["kv_pos"]) for c in calls],
-                                             q_pos=qmap, causal=w.causal, o=out, lse=lse))
-            else:
-                self.merge_bytes += out.numel() * out.element_size() + lse.numel() * 4
-                self.merges.append((o_parts, l_parts, out, lse))
+            row = 0
+            for qmap, nq in qsegs:
+                qs = q[row:row + nq]
+                o_parts, l_parts, seg_calls = [], [], []
+                for ci in order:
+                    src, lo, nk, kmap = plan[int(ci)]
+                    n_vis = cpa.visible_pairs(qmap, nq, kmap, nk, w.causal)
+                    if w.causal and n_vis == 0:
+                        continue  # chunk entirely in the future of this query block: never issued
+                    k, v = kv[src]
+                    o = torch.empty((nq, w.hq, w.d), dtype=o_dtype, device=dev)
+                    l = torch.empty((nq, w.hq), dtype=torch.float32, device=dev)
+                    seg_calls.append(dict(q=qs, k=k[lo:lo + nk], v=v[lo:lo + nk], q_pos=qmap,
+                                          kv_pos=kmap, causal=w.causal, o=o, lse=l))
+                    self.call_meta.append((qr, row, nq, src, lo, nk))
+                    self.flops += 4 * w.d * w.hq * n_vis
+                    o_parts.append(o)
+                    l_parts.append(l)
+                    fr = cpa.finite_rows(qmap, nq, kmap, nk, w.causal)
+                    self.merge_bytes += nq * w.hq * 4 + fr * w.hq * w.d * 4
+                o_seg, l_seg = out[row:row + nq], lse[row:row + nq]
+                if self.fused:
+                    # the block's chunks, in arrival order, in one launch; no partials, no merge
+                    self.fused_calls.append(dict(q=qs, chunks=[(c["k"], c["v"], c["kv_pos"]) for c in seg_calls],
+                                                 q_pos=qmap, causal=w.causal, o=o_seg, lse=l_seg))
+                    self.fused_meta.append(qr)
+                else:
+                    self.attn_calls += seg_calls
+                    self.merge_bytes += o_seg.numel() * o_seg.element_size() + l_seg.numel() * 4
+                    self.merges.append((o_parts, l_parts, o_seg, l_seg))
+                row += nq
             self._output_tensors += [out, lse]
-            self.rank_plans.append((qr, qmap, q, order))
+            self.rank_plans.append((qr, q, out, lse))
         if self.fused:
-            self.attn_calls = []  # the per-chunk partial buffers are not used
             self.merge_bytes = 0
 
     def _build_ulysses(self):
@@ -212,20 +232,32 @@ class Step:
             lib = cpa.load_library()
             import ctypes
             from context_blockwise_attention_gb300 import api
-            m = api._PosMap()
-            st = lib.cp_shard_layout(w.seq_len, w.cp, qr, api._LAYOUTS[self.layout],
-                                     ctypes.byref(m), ctypes.c_void_p(buf.data_ptr()),
-                                     ctypes.c_void_p(stream.cuda_stream))
+            maps = (api._PosMap * api.CP_MAX_SEGMENTS)()
+            lens = (ctypes.c_int64 * api.CP_MAX_SEGMENTS)()
+            nseg = ctypes.c_int32(0)
+            st = lib.cp_shard_segments(w.seq_len, w.cp, qr, api._LAYOUTS[self.layout], maps, lens,
+                                       ctypes.byref(nseg), ctypes.c_void_p(buf.data_ptr()),
+                                       ctypes.c_void_p(stream.cuda_stream))
             api._check(st)
-            n += 1
+            n += nseg.value
         t1 = ev() if timers is not None else None
-        for kw in self.attn_calls:
-            cpa.partial_attn(**kw)
-            n += 1
-        for kw in self.fused_calls:
-            cpa.partial_attn_chunks(**kw)
+        # with timers["rank_attn"], an event at every change of query rank gives each simulated
+        # rank's own attention time
+        per_rank = timers is not None and "rank_attn" in timers
+        launches = [(m[0], cpa.partial_attn, kw) for kw, m in zip(self.attn_calls, self.call_meta)]
+        launches += [(qr, cpa.partial_attn_chunks, kw) for kw, qr in zip(self.fused_calls, self.fused_meta)]
+        cur, start = None, None
+        for qr, fn, kw in launches:
+            if per_rank and qr != cur:
+                e = ev()
+                if cur is not None:
+                    timers["rank_attn"].append((cur, start, e))
+                cur, start = qr, e
+            fn(**kw)
             n += 1
         t2 = ev() if timers is not None else None
+        if per_rank and cur is not None:
+            timers["rank_attn"].append((cur, start, t2))
         for o_parts, l_parts, out, lse in self.merges:
             cpa.merge_partials(o_parts, l_parts, o=out, lse=lse)
             n += 1
@@ -411,6 +443,9 @@ def _config_dict(w, layout, extra):
          "cp": w.cp, "hq": w.hq, "hkv": w.hkv, "head_dim": w.d, "causal": w.causal,
          "chunks": w.n_chunks, "chunk_tokens": w.chunk_len,
          "l2": "flushed (512 MiB write) before every timed step"}
+    if layout == "two_block" and w.chunk_len > w.local_len // 2:
+        # a chunk never straddles the two blocks of a shard
+        d.update(chunks=2 * w.cp, chunk_tokens=w.local_len // 2)
     d.update(extra)
     return d
 
@@ -423,11 +458,11 @@ def run_reference(args):
         return
     rows = args.ref_rows
     for _ in range(args.warmup):
-        oracle_sample(args.config, max(1, rows // 4))
+        oracle_sample(args.config, max(1, rows // 4), layout=args.layout)
     times, fl = [], 0
     desc = ""
     for _ in range(args.steps):
-        t, fl, desc = oracle_sample(args.config, rows)
+        t, fl, desc = oracle_sample(args.config, rows, layout=args.layout)
         times.append(t)
     tmean = sum(times) / len(times)
     value = fl / tmean / 1e12
@@ -474,6 +509,8 @@ def run_gpu(args):
 
     # ---- device-timed steps (inputs resident), L2 flushed before each
     timers = {"attn": [], "merge": [], "reshard": []}
+    if len(step.rank_plans) > 1:
+        timers["rank_attn"] = []
     sampler = ClockSampler(local)
     sampler.start()
     step_ms, launches = [], 0
@@ -528,6 +565,16 @@ def run_gpu(args):
                 "traffic": traffic}
     extra = {"attn_ms_per_step": attn_ms, "attn_tflops": achieved,
              "step_flop": step.flops, "query_rank": qr}
+    if timers.get("rank_attn"):
+        # every simulated rank's attention time: with one GPU per rank the step would wait for
+        # the slowest, so max / mean shows the layout's load balance
+        per = {}
+        for r_, s_, e_ in timers["rank_attn"]:
+            per[r_] = per.get(r_, 0.0) + s_.elapsed_time(e_) / args.steps
+        ms = [per[r_] for r_ in sorted(per)]
+        extra["per_rank_attn_ms"] = ms
+        extra["simulated_parallel_attn_ms"] = max(ms)
+        extra["rank_balance_max_over_mean"] = max(ms) / (sum(ms) / len(ms))
     if merge_ms:
         gbs = step.merge_bytes / (merge_ms * 1e-3) / 1e9
         extra["merge"] = {"ms": merge_ms, "GB/s": gbs, "frac": gbs / peaks["hbm"],
@@ -561,11 +608,11 @@ def run_gpu(args):
         fused = {"value": f_value, "unit": "TFLOP/s", "ms_per_step": f_ms,
                  "attn_tflops": f_ach, "attn_frac": f_ach / peaks["bf16"],
                  "launches_per_step": len(fstep.fused_calls),
-                 "path": "one cp_partial_attn_chunks per query rank (no partials, no merge)"}
+                 "path": "one cp_partial_attn_chunks per query block (no partials, no merge)"}
         del fstep
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        t, fl, desc = oracle_sample(args.config, args.ref_rows)
+        t, fl, desc = oracle_sample(args.config, args.ref_rows, layout=layout)
         cpu = {"value": fl / t / 1e12, "unit": "TFLOP/s", "cores": _blas_threads(),
                "kind": "oracle", "sample": desc, "seconds": t}
     if rank == 0:
@@ -737,7 +784,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
-    ap.add_argument("--layout", default=None, choices=[None, "contiguous", "strided"])
+    ap.add_argument("--layout", default=None, choices=[None, "contiguous", "strided", "two_block"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--ref-rows", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")

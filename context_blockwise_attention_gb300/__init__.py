@@ -10,6 +10,7 @@ from .api import (  # noqa: F401
     CpError,
     PosMap,
     shard_layout,
+    shard_segments,
     sub_chunk_map,
     partial_attn,
     partial_attn_chunks,
@@ -26,6 +27,7 @@ __all__ = [
     "CpError",
     "PosMap",
     "shard_layout",
+    "shard_segments",
     "sub_chunk_map",
     "partial_attn",
     "partial_attn_chunks",

@@ -14,7 +14,8 @@ import torch
 from . import build as _build
 
 CP_OK, CP_ERR_INVALID_ARG, CP_ERR_UNSUPPORTED, CP_ERR_CUDA, CP_ERR_TIMEOUT = range(5)
-CP_LAYOUT_CONTIGUOUS, CP_LAYOUT_STRIDED = 0, 1
+CP_LAYOUT_CONTIGUOUS, CP_LAYOUT_STRIDED, CP_LAYOUT_TWO_BLOCK = 0, 1, 2
+CP_MAX_SEGMENTS = 2
 CP_F32, CP_BF16 = 0, 1
 CP_FLAG_KV_DESCENDING = 0x1
 CP_FLAG_TEST_STALL = 0x100
@@ -22,7 +23,8 @@ CP_MAX_PARTIALS = 128
 CP_MAX_CHUNKS = 64
 
 _LAYOUTS = {"contiguous": CP_LAYOUT_CONTIGUOUS, "strided": CP_LAYOUT_STRIDED,
-            CP_LAYOUT_CONTIGUOUS: CP_LAYOUT_CONTIGUOUS, CP_LAYOUT_STRIDED: CP_LAYOUT_STRIDED}
+            "two_block": CP_LAYOUT_TWO_BLOCK, CP_LAYOUT_CONTIGUOUS: CP_LAYOUT_CONTIGUOUS,
+            CP_LAYOUT_STRIDED: CP_LAYOUT_STRIDED, CP_LAYOUT_TWO_BLOCK: CP_LAYOUT_TWO_BLOCK}
 
 
 class CpError(RuntimeError):
@@ -84,6 +86,9 @@ def load_library():
     lib.cp_last_error.argtypes = []
     lib.cp_shard_layout.restype = i32
     lib.cp_shard_layout.argtypes = [i64, i32, i32, i32, ctypes.POINTER(_PosMap), vp, vp]
+    lib.cp_shard_segments.restype = i32
+    lib.cp_shard_segments.argtypes = [i64, i32, i32, i32, ctypes.POINTER(_PosMap),
+                                      ctypes.POINTER(i64), ctypes.POINTER(i32), vp, vp]
     lib.cp_partial_attn.restype = i32
     lib.cp_partial_attn.argtypes = [ctypes.POINTER(_AttnDesc), vp]
     lib.cp_partial_attn_chunks.restype = i32
@@ -149,6 +154,30 @@ def shard_layout(seq_len, cp, rank, kind="contiguous", positions=False, device=N
                                ctypes.byref(m), ptr, _stream(stream) if positions else None))
     pm = PosMap(m.base, m.stride)
     return (pm, out) if positions else pm
+
+
+def shard_segments(seq_len, cp, rank, kind="contiguous", positions=False, device=None, stream=None):
+    """The shard of rank ``rank`` as a list of ``(PosMap, length)`` affine segments in local
+    order (two for the two-block layout, one otherwise); with ``positions=True`` also an int32
+    CUDA tensor of every local token's position, filled by the library's kernel."""
+    lib = load_library()
+    maps = (_PosMap * CP_MAX_SEGMENTS)()
+    lens = (ctypes.c_int64 * CP_MAX_SEGMENTS)()
+    n = ctypes.c_int32(0)
+    out = None
+    ptr = None
+    if positions:
+        # validate first so that a bad shape fails before anything is allocated
+        _check(lib.cp_shard_segments(int(seq_len), int(cp), int(rank), _LAYOUTS.get(kind, -1),
+                                     maps, lens, ctypes.byref(n), None, None))
+        device = device or torch.device("cuda", torch.cuda.current_device())
+        out = torch.empty(int(seq_len) // int(cp), dtype=torch.int32, device=device)
+        ptr = ctypes.c_void_p(out.data_ptr())
+    _check(lib.cp_shard_segments(int(seq_len), int(cp), int(rank), _LAYOUTS.get(kind, -1),
+                                 maps, lens, ctypes.byref(n), ptr,
+                                 _stream(stream) if positions else None))
+    segs = [(PosMap(maps[i].base, maps[i].stride), int(lens[i])) for i in range(n.value)]
+    return (segs, out) if positions else segs
 
 
 def sub_chunk_map(shard: PosMap, index: int, length: int) -> PosMap:

@@ -83,35 +83,90 @@ CP_API int32_t cp_version(void) { return CP_ABI_VERSION; }
 
 CP_API const char* cp_last_error(void) { return cpattn::g_err; }
 
+// The affine segments of rank `rank`'s shard under layout `kind`, in local order.
+static cp_status shard_segments(const char* who, int64_t seq_len, int32_t cp, int32_t rank,
+                                int32_t kind, cp_posmap* maps, int64_t* lens, int32_t* n) {
+  if (seq_len <= 0) CP_INVALID("%s: seq_len must be positive (got %lld)", who, (long long)seq_len);
+  if (cp <= 0) CP_INVALID("%s: cp must be positive (got %d)", who, cp);
+  if (rank < 0 || rank >= cp) CP_INVALID("%s: rank %d not in [0, %d)", who, rank, cp);
+  if (seq_len % cp != 0)
+    CP_INVALID("%s: seq_len %lld is not a multiple of cp %d", who, (long long)seq_len, cp);
+  const int64_t local = seq_len / cp;
+  if (kind == CP_LAYOUT_CONTIGUOUS) {
+    maps[0] = cp_posmap{static_cast<int64_t>(rank) * local, 1};
+    lens[0] = local;
+    *n = 1;
+  } else if (kind == CP_LAYOUT_STRIDED) {
+    maps[0] = cp_posmap{rank, cp};
+    lens[0] = local;
+    *n = 1;
+  } else if (kind == CP_LAYOUT_TWO_BLOCK) {
+    if (seq_len % (2 * static_cast<int64_t>(cp)) != 0)
+      CP_INVALID("%s: the two-block split needs seq_len %lld to be a multiple of 2*cp = %d", who,
+                 (long long)seq_len, 2 * cp);
+    const int64_t b = local / 2;
+    maps[0] = cp_posmap{static_cast<int64_t>(rank) * b, 1};
+    maps[1] = cp_posmap{static_cast<int64_t>(2 * cp - 1 - rank) * b, 1};
+    lens[0] = lens[1] = b;
+    *n = 2;
+  } else {
+    CP_INVALID("%s: unknown layout kind %d", who, kind);
+  }
+  return CP_OK;
+}
+
+static cp_status fill_segments(const char* who, int64_t seq_len, const cp_posmap* maps,
+                               const int64_t* lens, int32_t n, int32_t* dev_positions_out,
+                               cudaStream_t stream) {
+  if (dev_positions_out == nullptr) return CP_OK;
+  if (seq_len > INT32_MAX) CP_INVALID("%s: int32 positions need seq_len <= INT32_MAX", who);
+  cp_status st = require_sm103(nullptr, nullptr);
+  if (st != CP_OK) return st;
+  int64_t off = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    st = launch_fill_positions(dev_positions_out + off, lens[i], maps[i].base, maps[i].stride, stream);
+    if (st != CP_OK) return st;
+    off += lens[i];
+  }
+  return CP_OK;
+}
+
 CP_API cp_status cp_shard_layout(int64_t seq_len, int32_t cp, int32_t rank, int32_t kind,
                                  cp_posmap* map_out, int32_t* dev_positions_out,
                                  cudaStream_t stream) {
   clear_error();
   if (map_out == nullptr) CP_INVALID("cp_shard_layout: map_out is NULL");
-  if (seq_len <= 0) CP_INVALID("cp_shard_layout: seq_len must be positive (got %lld)", (long long)seq_len);
-  if (cp <= 0) CP_INVALID("cp_shard_layout: cp must be positive (got %d)", cp);
-  if (rank < 0 || rank >= cp) CP_INVALID("cp_shard_layout: rank %d not in [0, %d)", rank, cp);
-  if (seq_len % cp != 0)
-    CP_INVALID("cp_shard_layout: seq_len %lld is not a multiple of cp %d", (long long)seq_len, cp);
-  const int64_t local = seq_len / cp;
-  cp_posmap m;
-  if (kind == CP_LAYOUT_CONTIGUOUS) {
-    m.base = static_cast<int64_t>(rank) * local;
-    m.stride = 1;
-  } else if (kind == CP_LAYOUT_STRIDED) {
-    m.base = rank;
-    m.stride = cp;
-  } else {
-    CP_INVALID("cp_shard_layout: unknown layout kind %d", kind);
+  cp_posmap maps[CP_MAX_SEGMENTS];
+  int64_t lens[CP_MAX_SEGMENTS];
+  int32_t n = 0;
+  cp_status st = shard_segments("cp_shard_layout", seq_len, cp, rank, kind, maps, lens, &n);
+  if (st != CP_OK) return st;
+  if (n != 1)
+    CP_INVALID("cp_shard_layout: layout %d has %d affine segments; use cp_shard_segments", kind, n);
+  st = fill_segments("cp_shard_layout", seq_len, maps, lens, n, dev_positions_out, stream);
+  if (st != CP_OK) return st;
+  *map_out = maps[0];
+  return CP_OK;
+}
+
+CP_API cp_status cp_shard_segments(int64_t seq_len, int32_t cp, int32_t rank, int32_t kind,
+                                   cp_posmap* maps_out, int64_t* lens_out, int32_t* n_segments_out,
+                                   int32_t* dev_positions_out, cudaStream_t stream) {
+  clear_error();
+  if (maps_out == nullptr || lens_out == nullptr || n_segments_out == nullptr)
+    CP_INVALID("cp_shard_segments: maps_out, lens_out and n_segments_out must not be NULL");
+  cp_posmap maps[CP_MAX_SEGMENTS];
+  int64_t lens[CP_MAX_SEGMENTS];
+  int32_t n = 0;
+  cp_status st = shard_segments("cp_shard_segments", seq_len, cp, rank, kind, maps, lens, &n);
+  if (st != CP_OK) return st;
+  st = fill_segments("cp_shard_segments", seq_len, maps, lens, n, dev_positions_out, stream);
+  if (st != CP_OK) return st;
+  for (int32_t i = 0; i < n; ++i) {
+    maps_out[i] = maps[i];
+    lens_out[i] = lens[i];
   }
-  if (dev_positions_out != nullptr) {
-    if (seq_len > INT32_MAX) CP_INVALID("cp_shard_layout: int32 positions need seq_len <= INT32_MAX");
-    cp_status st = require_sm103(nullptr, nullptr);
-    if (st != CP_OK) return st;
-    st = launch_fill_positions(dev_positions_out, local, m.base, m.stride, stream);
-    if (st != CP_OK) return st;
-  }
-  *map_out = m;
+  *n_segments_out = n;
   return CP_OK;
 }
 
@@ -246,7 +301,10 @@ CP_API cp_status cp_ulysses_reshard(int32_t dir, int32_t cp, int64_t seq_len, in
   if (d <= 0) CP_INVALID("cp_ulysses_reshard: d must be positive");
   const int64_t es = dtype_size(dtype);
   if (es == 0) CP_INVALID("cp_ulysses_reshard: bad dtype %d", dtype);
-  if (layout != CP_LAYOUT_CONTIGUOUS && layout != CP_LAYOUT_STRIDED) CP_INVALID("cp_ulysses_reshard: bad layout %d", layout);
+  if (layout != CP_LAYOUT_CONTIGUOUS && layout != CP_LAYOUT_STRIDED && layout != CP_LAYOUT_TWO_BLOCK)
+    CP_INVALID("cp_ulysses_reshard: bad layout %d", layout);
+  if (layout == CP_LAYOUT_TWO_BLOCK && seq_len % (2 * static_cast<int64_t>(cp)) != 0)
+    CP_INVALID("cp_ulysses_reshard: the two-block split needs seq_len to be a multiple of 2*cp");
   if (cp > 64) CP_INVALID("cp_ulysses_reshard: cp must be <= 64");
   for (int t = 0; t < n_tensors; ++t) {
     if (heads[t] <= 0 || heads[t] % cp != 0) CP_INVALID("cp_ulysses_reshard: heads[%d]=%d not a positive multiple of cp %d", t, heads[t], cp);

@@ -9,7 +9,8 @@
 //
 // Bandwidth-bound: each 16-byte vector is read once and written once.  The walk is linear over
 // the sequence-sharded side (X), so one side is fully sequential; on the head-sharded side
-// each (token, rank) segment of (H/cp)*d elements is contiguous.
+// each (token, rank) segment of (H/cp)*d elements is contiguous.  Shard layouts: contiguous,
+// strided, or two blocks per rank (blocks r and 2cp-1-r of S/(2cp) tokens).
 #include "internal.h"
 
 namespace cpattn {
@@ -23,8 +24,11 @@ struct ReshardParams {
   int64_t row_vecs[kMaxReshardTensors];  // H_t * d * esize / 16  (one token of X)
   int64_t seg_vecs[kMaxReshardTensors];  // row_vecs / cp         (one rank's head block)
   int64_t local;                         // S / cp
-  int64_t pos_base_step;                 // contiguous: local; strided: 1   (base = s * step)
-  int64_t pos_stride;                    // contiguous: 1;     strided: cp
+  // Shard s's positions: local token i < seg0 is at s * pos_base_step + pos_stride * i; the
+  // rest (two-block layout only) at (2cp - 1 - s) * seg0 + (i - seg0).
+  int64_t seg0;                          // contiguous / strided: local;  two-block: local / 2
+  int64_t pos_base_step;                 // contiguous: local; strided: 1; two-block: local / 2
+  int64_t pos_stride;                    // contiguous: 1;     strided: cp; two-block: 1
   int32_t cp;
   int32_t dir;
 };
@@ -44,7 +48,8 @@ __global__ void __launch_bounds__(256) reshard_kernel(const __grid_constant__ Re
     const int64_t rem = g - i * row_vecs;
     const int64_t r = rem / seg_vecs;      // head-rank
     const int64_t v = rem - r * seg_vecs;  // vector inside the head block
-    const int64_t pos = pos_base + p.pos_stride * i;
+    const int64_t pos = i < p.seg0 ? pos_base + p.pos_stride * i
+                                   : (2 * p.cp - 1 - s) * p.seg0 + (i - p.seg0);
     const int64_t y_off = pos * seg_vecs + v;
     if (p.dir == 0) {
       const uint4 x = __ldcs(p.in[ts] + g);
@@ -72,12 +77,17 @@ cp_status launch_reshard(const ReshardArgs& a, int num_sms, cudaStream_t s) {
     }
   }
   p.local = a.seq_len / a.cp;
+  p.seg0 = p.local;
   if (a.layout == CP_LAYOUT_CONTIGUOUS) {
     p.pos_base_step = p.local;
     p.pos_stride = 1;
-  } else {
+  } else if (a.layout == CP_LAYOUT_STRIDED) {
     p.pos_base_step = 1;
     p.pos_stride = a.cp;
+  } else {  // two blocks: r and 2cp - 1 - r
+    p.seg0 = p.local / 2;
+    p.pos_base_step = p.seg0;
+    p.pos_stride = 1;
   }
   p.cp = a.cp;
   p.dir = a.dir;

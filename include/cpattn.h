@@ -32,7 +32,7 @@
 extern "C" {
 #endif
 
-#define CP_ABI_VERSION 1
+#define CP_ABI_VERSION 2
 /* Largest number of partials one cp_merge_partials call accepts. */
 #define CP_MAX_PARTIALS 128
 
@@ -44,7 +44,14 @@ typedef enum {
   CP_ERR_TIMEOUT = 4      /* a bounded in-kernel wait expired (reported via *status)     */
 } cp_status;
 
-typedef enum { CP_LAYOUT_CONTIGUOUS = 0, CP_LAYOUT_STRIDED = 1 } cp_layout;
+typedef enum {
+  CP_LAYOUT_CONTIGUOUS = 0, /* one block of seq_len/cp tokens per rank                       */
+  CP_LAYOUT_STRIDED = 1,    /* every cp-th token ("zig-zag" on the pages)                    */
+  CP_LAYOUT_TWO_BLOCK = 2   /* blocks r and 2cp-1-r of seq_len/(2cp) tokens (two segments)   */
+} cp_layout;
+
+/* Most affine segments a shard layout has (cp_shard_segments). */
+#define CP_MAX_SEGMENTS 2
 typedef enum { CP_F32 = 0, CP_BF16 = 1 } cp_dtype;
 
 /* Global position of local token i: base + stride * i. */
@@ -70,6 +77,30 @@ typedef struct {
  */
 cp_status cp_shard_layout(int64_t seq_len, int32_t cp, int32_t rank, int32_t kind,
                           cp_posmap* map_out, int32_t* dev_positions_out, cudaStream_t stream);
+
+/*
+ * cp_shard_segments -- the same question for any layout, answered as a list of affine segments
+ * in local order (local tokens [0, lens[0]) follow maps[0], the next lens[1] follow maps[1]).
+ *   CP_LAYOUT_CONTIGUOUS, CP_LAYOUT_STRIDED: one segment, the cp_shard_layout map.
+ *   CP_LAYOUT_TWO_BLOCK: [ZigZag] sections 4.2 / 5.2 give the aim of the zig-zag split (every
+ *     rank gets early and late tokens, so causal work is even); this is its block-granular form,
+ *     which the pages do not print: 2*cp blocks of b = seq_len/(2cp) tokens, rank r holds block r
+ *     then block 2cp-1-r -- maps {r*b, 1} and {(2cp-1-r)*b, 1}, b tokens each.  Every rank then
+ *     sees exactly b*b*(2cp-1) + b*(b+1) causal pairs.  Needs seq_len % (2*cp) == 0.
+ * Arguments:
+ *   seq_len, cp, rank, kind   as cp_shard_layout.
+ *   maps_out, lens_out        host arrays [CP_MAX_SEGMENTS], required; entries past the count
+ *                             are left untouched.
+ *   n_segments_out            host pointer, required: 1 or 2.
+ *   dev_positions_out         device int32 [seq_len/cp] or NULL: every local token's position,
+ *                             written on `stream` (requires seq_len <= INT32_MAX).
+ * Errors: CP_ERR_INVALID_ARG as cp_shard_layout (and seq_len % (2cp) != 0 for the two-block
+ *         split); CP_ERR_CUDA if the fill kernel fails to launch.
+ * cp_shard_layout rejects CP_LAYOUT_TWO_BLOCK (it is not one affine map).
+ */
+cp_status cp_shard_segments(int64_t seq_len, int32_t cp, int32_t rank, int32_t kind,
+                            cp_posmap* maps_out, int64_t* lens_out, int32_t* n_segments_out,
+                            int32_t* dev_positions_out, cudaStream_t stream);
 
 /* Flags for cp_attn_desc.flags. */
 #define CP_FLAG_KV_DESCENDING 0x1 /* visit the chunk's KV tiles last-to-first (same result)   */
@@ -197,7 +228,7 @@ cp_status cp_merge_partials(int32_t n, const float* const* o_parts, const float*
  *   heads      host array [n_tensors]: full head count H_t of each tensor; H_t % cp == 0
  *   d          head_dim; (H_t/cp) * d * sizeof(dtype) must be a multiple of 16 bytes
  *   dtype      CP_F32 or CP_BF16
- *   layout     cp_layout of the sequence shards
+ *   layout     cp_layout of the sequence shards (CP_LAYOUT_TWO_BLOCK needs seq_len % (2cp) == 0)
  *   in, out    host arrays [n_tensors*cp] of device pointers (16-byte aligned), shapes above
  * Bit-exact copy.  Errors: CP_ERR_INVALID_ARG, CP_ERR_CUDA.
  */

@@ -45,38 +45,43 @@ def _check_rank_workload(cfg, layout, sample, query_ranks=None):
         for kw in step.attn_calls:  # poison outputs so unwritten rows cannot pass
             kw["o"].fill_(float("nan"))
             kw["lse"].fill_(float("nan"))
+        for _, _, out, lse in step.rank_plans:
+            out.fill_(float("nan"))
+            lse.fill_(float("nan"))
         step.run()
         torch.cuda.synchronize()
         steps.append(step)
     kv_cpu = {r: (k.cpu(), v.cpu()) for r, (k, v) in steps[0].kv.items()}
+    shard_pos = {r: oracle.shard_positions(w.seq_len, w.cp, r, layout) for r in range(w.cp)}
+    all_k = torch.cat([kv_cpu[r][0] for r in range(w.cp)])
+    all_v = torch.cat([kv_cpu[r][1] for r in range(w.cp)])
+    all_pos = np.concatenate([shard_pos[r] for r in range(w.cp)])
     worst = [0.0, 0.0]
     for step in steps:
-        for (qr, qmap, q, order), (o_parts, l_parts, out, lse) in zip(step.rank_plans, step.merges):
-            qpos = oracle.shard_positions(w.seq_len, w.cp, qr, layout)
+        for qr, q, out, lse in step.rank_plans:
+            qpos = shard_pos[qr]
             rows = _rows_for(w, w.local_len + qr, sample)
-            q_rows = q[torch.from_numpy(rows).to(DEV)].cpu()
-            calls = [(i, m) for i, m in enumerate(step.call_meta) if m[0] == qr]
-            all_k, all_v, all_pos = [], [], []
-            for src in range(w.cp):
-                spos = oracle.shard_positions(w.seq_len, w.cp, src, layout)
-                all_k.append(kv_cpu[src][0])
-                all_v.append(kv_cpu[src][1])
-                all_pos.append(spos)
-            # every partial on the sampled rows
-            for i, (_, src, sub) in calls:
+            q_cpu = q.cpu()
+            # every partial on the sampled rows of its query block; positions from the oracle's
+            # own layout, cut to the call's row ranges
+            for i, (cqr, row, nq, src, lo, nk) in enumerate(step.call_meta):
+                if cqr != qr:
+                    continue
                 kw = step.attn_calls[i]
-                kpos = oracle.sub_chunk_positions(
-                    oracle.shard_positions(w.seq_len, w.cp, src, layout), sub, w.chunk_len)
-                lo, hi = sub * w.chunk_len, (sub + 1) * w.chunk_len
-                o_ref, l_ref = oracle.attention(q_rows, kv_cpu[src][0][lo:hi], kv_cpu[src][1][lo:hi],
-                                                qpos[rows], kpos, causal=w.causal)
-                idx = torch.from_numpy(rows).to(DEV)
+                sel = rows[(rows >= row) & (rows < row + nq)]
+                if len(sel) == 0:
+                    continue
+                o_ref, l_ref = oracle.attention(q_cpu[sel], kv_cpu[src][0][lo:lo + nk],
+                                                kv_cpu[src][1][lo:lo + nk], qpos[sel],
+                                                shard_pos[src][lo:lo + nk], causal=w.causal)
+                idx = torch.from_numpy(sel - row).to(DEV)
                 eo, el = compare_partial(kw["o"][idx].float().cpu().numpy(), kw["lse"][idx].cpu().numpy(),
-                                         o_ref, l_ref, tol_o, tol_l, f"cfg{cfg} rank{qr} chunk({src},{sub})")
+                                         o_ref, l_ref, tol_o, tol_l,
+                                         f"cfg{cfg} rank{qr} rows {row}+ chunk({src},{lo})")
                 worst = [max(worst[0], eo), max(worst[1], el)]
             # merged output against unsharded attention over every key
-            o_ref, l_ref = oracle.attention(q_rows, torch.cat(all_k), torch.cat(all_v), qpos[rows],
-                                            np.concatenate(all_pos), causal=w.causal)
+            o_ref, l_ref = oracle.attention(q_cpu[rows], all_k, all_v, qpos[rows], all_pos,
+                                            causal=w.causal)
             idx = torch.from_numpy(rows).to(DEV)
             eo, el = compare_partial(out[idx].float().cpu().numpy(), lse[idx].cpu().numpy(), o_ref,
                                      l_ref, tol_o, tol_l, f"cfg{cfg} rank{qr} merged")
@@ -99,7 +104,7 @@ def test_cfg2_rank0_sampled():
     _check_rank_workload(2, "strided", 256, query_ranks=[0])
 
 
-@pytest.mark.parametrize("layout", ["strided", "contiguous"])
+@pytest.mark.parametrize("layout", ["strided", "contiguous", "two_block"])
 def test_cfg3_all_ranks_sampled(layout):
     _check_rank_workload(3, layout, 128)
 
@@ -111,27 +116,32 @@ def test_cfg5_rank7_sampled_outliers():
 def _check_fused(cfg, layout, sample):
     w = wl.WORKLOADS[cfg]
     step = bench.Step(cfg, DEV, layout=layout, fused=True)
-    for kw in step.fused_calls:
-        kw["o"].fill_(float("nan"))
-        kw["lse"].fill_(float("nan"))
+    for _, _, out, lse in step.rank_plans:
+        out.fill_(float("nan"))
+        lse.fill_(float("nan"))
     step.run()
     torch.cuda.synchronize()
     kv_cpu = {r: (k.cpu(), v.cpu()) for r, (k, v) in step.kv.items()}
     all_k = torch.cat([kv_cpu[r][0] for r in range(w.cp)])
     all_v = torch.cat([kv_cpu[r][1] for r in range(w.cp)])
     all_pos = np.concatenate([oracle.shard_positions(w.seq_len, w.cp, r, layout) for r in range(w.cp)])
-    for (qr, qmap, q, order), kw in zip(step.rank_plans, step.fused_calls):
+    for qr, q, out, lse in step.rank_plans:
         qpos = oracle.shard_positions(w.seq_len, w.cp, qr, layout)
         rows = _rows_for(w, w.local_len + qr, sample)
         idx = torch.from_numpy(rows).to(DEV)
         o_ref, l_ref = oracle.attention(q[idx].cpu(), all_k, all_v, qpos[rows], all_pos, causal=w.causal)
-        compare_partial(kw["o"][idx].float().cpu().numpy(), kw["lse"][idx].cpu().numpy(), o_ref, l_ref,
+        compare_partial(out[idx].float().cpu().numpy(), lse[idx].cpu().numpy(), o_ref, l_ref,
                         TOL_BF16_O, TOL_BF16_LSE, f"cfg{cfg} fused rank{qr}")
 
 
 def test_cfg2_fused_full():
     # one launch consumes the 8 chunks in arrival order; every row and head
     _check_fused(2, "strided", None)
+
+
+def test_cfg3_two_block_fused_sampled():
+    # two query blocks per rank, each one launch over the 16 KV blocks visible to it
+    _check_fused(3, "two_block", 128)
 
 
 def test_cfg5_fused_sampled():

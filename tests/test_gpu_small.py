@@ -129,6 +129,61 @@ def test_layout_positions_bit_exact(kind):
             assert np.array_equal(_pos(m, len(ref)), ref)
 
 
+def test_segments_positions_bit_exact():
+    for kind in ("contiguous", "strided", "two_block"):
+        for seq, cp in ((64, 4), (32768, 8), (131072, 4), (16, 8)):
+            for r in range(cp):
+                segs, pos = cpa.shard_segments(seq, cp, r, kind, positions=True)
+                ref = oracle.shard_positions(seq, cp, r, kind)
+                assert np.array_equal(pos.cpu().numpy().astype(np.int64), ref)
+                assert np.array_equal(np.concatenate([_pos(m, n) for m, n in segs]), ref)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_two_block_layout_attention(d):
+    # every rank of a two-block split: each query segment against every rank's KV segments,
+    # fused (one call per query segment) and as partials + merge; the union over ranks is the
+    # unsharded causal attention
+    seq, cp, hq, hkv = 2048, 4, 4, 2
+    qf = wl.normal((seq, hq, d), torch.bfloat16, 501, 0.5, device=DEV)
+    kf = wl.normal((seq, hkv, d), torch.bfloat16, 502, 0.5, device=DEV)
+    vf = wl.normal((seq, hkv, d), torch.bfloat16, 503, 1.0, device=DEV)
+    o_ref, l_ref = oracle.attention(qf.cpu(), kf.cpu(), vf.cpu(), np.arange(seq), np.arange(seq),
+                                    causal=True)
+    segs = [cpa.shard_segments(seq, cp, r, "two_block") for r in range(cp)]
+    kv_chunks = []
+    for r in range(cp):
+        for m, n in segs[r]:
+            kv_chunks.append((kf[m.base:m.base + n].contiguous(), vf[m.base:m.base + n].contiguous(), m))
+    order = np.random.default_rng(5).permutation(len(kv_chunks))
+    for r in range(cp):
+        pos = np.concatenate([_pos(m, n) for m, n in segs[r]])
+        q = qf[torch.from_numpy(pos).to(DEV)].contiguous()
+        o_fused = torch.full((len(pos), hq, d), float("nan"), device=DEV)
+        l_fused = torch.full((len(pos), hq), float("nan"), device=DEV)
+        parts = []
+        row = 0
+        for m, n in segs[r]:
+            cpa.partial_attn_chunks(q[row:row + n], [kv_chunks[i] for i in order], m,
+                                    o=o_fused[row:row + n], lse=l_fused[row:row + n])
+            row += n
+        for i in order:
+            k, v, km = kv_chunks[i]
+            o_p = torch.full((len(pos), hq, d), float("nan"), device=DEV)
+            l_p = torch.full((len(pos), hq), float("nan"), device=DEV)
+            row = 0
+            for m, n in segs[r]:
+                cpa.partial_attn(q[row:row + n], k, v, m, km, o=o_p[row:row + n], lse=l_p[row:row + n])
+                row += n
+            parts.append((o_p, l_p))
+        o_m, l_m = cpa.merge_partials([p[0] for p in parts], [p[1] for p in parts],
+                                      out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        for o, l, what in ((o_fused, l_fused, "fused"), (o_m, l_m, "partials+merge")):
+            compare_partial(o.cpu().numpy(), l.cpu().numpy(), o_ref[pos], l_ref[pos],
+                            TOL_BF16_O, TOL_BF16_LSE, f"two-block rank {r} {what} d={d}")
+
+
 # ------------------------------------------------------------------------------- merge
 
 def _random_partials(n, sq, h, d, seed, empty_frac=0.3, spread=4.0):
@@ -186,7 +241,7 @@ def test_merge_order_independent_and_associative():
 
 # ------------------------------------------------------------------------------- reshard
 
-@pytest.mark.parametrize("kind", ["contiguous", "strided"])
+@pytest.mark.parametrize("kind", ["contiguous", "strided", "two_block"])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_reshard_bit_exact(kind, dtype):
     seq, cp, d = 512, 4, 64

@@ -23,7 +23,7 @@ def test_exports_every_declared_function():
 
 
 def test_version():
-    assert cpa.version() == 1
+    assert cpa.version() == 2
 
 
 def test_desc_layout_matches_header():
@@ -152,3 +152,58 @@ def test_partial_attn_chunks_rejects():
     ch[1].k = 0x1008
     assert lib.cp_partial_attn_chunks(ctypes.byref(d), 2, ch, None) == api.CP_ERR_INVALID_ARG
     assert b"chunk 1" in lib.cp_last_error()
+
+
+def _segments(seq, cp, rank, kind):
+    lib = cpa.load_library()
+    maps = (api._PosMap * api.CP_MAX_SEGMENTS)()
+    lens = (ctypes.c_int64 * api.CP_MAX_SEGMENTS)()
+    n = ctypes.c_int32(-1)
+    st = lib.cp_shard_segments(seq, cp, rank, kind, maps, lens, ctypes.byref(n), None, None)
+    return st, [(maps[i].base, maps[i].stride, lens[i]) for i in range(max(n.value, 0))]
+
+
+@pytest.mark.parametrize("seq,cp,rank,kind", [
+    (60, 4, 0, 2),    # two blocks need seq % (2 cp) == 0
+    (12, 8, 0, 2),    # not even a multiple of cp
+    (64, 4, 4, 2),
+    (64, 4, 0, 9),
+])
+def test_segments_reject(seq, cp, rank, kind):
+    st, _ = _segments(seq, cp, rank, kind)
+    assert st == api.CP_ERR_INVALID_ARG and cpa.load_library().cp_last_error()
+
+
+def test_segments_reject_null_outputs_and_single_map_call():
+    lib = cpa.load_library()
+    maps = (api._PosMap * api.CP_MAX_SEGMENTS)()
+    n = ctypes.c_int32()
+    assert lib.cp_shard_segments(64, 4, 0, 2, maps, None, ctypes.byref(n), None, None) == \
+        api.CP_ERR_INVALID_ARG
+    # the two-block split is not one affine map
+    assert _layout(64, 4, 0, api.CP_LAYOUT_TWO_BLOCK)[0] == api.CP_ERR_INVALID_ARG
+
+
+def test_segments_host_maps_equal_oracle_positions():
+    # host-only: the segments' affine maps, expanded, are the oracle's positions exactly
+    import numpy as np
+    import oracle
+    for kind_name, kind in (("contiguous", 0), ("strided", 1), ("two_block", 2)):
+        for seq, cp in ((64, 4), (48, 8), (32768, 8), (131072, 4), (16, 1)):
+            for r in range(cp):
+                st, segs = _segments(seq, cp, r, kind)
+                assert st == 0
+                assert len(segs) == (2 if kind == 2 else 1)
+                got = np.concatenate([b + s * np.arange(n, dtype=np.int64) for b, s, n in segs])
+                assert np.array_equal(got, oracle.shard_positions(seq, cp, r, kind_name))
+    st, _ = _layout(64, 4, 0, 0)
+    assert st == 0
+
+
+def test_reshard_rejects_two_block_odd_length():
+    lib = cpa.load_library()
+    ptrs = (ctypes.c_void_p * 4)(0x1000, 0x2000, 0x3000, 0x4000)
+    heads = (ctypes.c_int32 * 1)(8)
+    # 36 % 4 == 0 but 36 % 8 != 0
+    assert lib.cp_ulysses_reshard(0, 4, 36, 1, heads, 64, 1, api.CP_LAYOUT_TWO_BLOCK, ptrs, ptrs,
+                                  None) == api.CP_ERR_INVALID_ARG
