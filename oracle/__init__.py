@@ -22,12 +22,16 @@ Sources (pages are cited by title and section):
 * "Halo context parallelism (CP + Ulysses attention)" (sheratonhq.com/news/191935), section
   "Ulysses attention: three all-to-alls for one exact computation": each rank holds S/cp tokens
   of all heads; the exchange gives it all S tokens of H/cp heads; exact because heads are
-  independent.  Example: cp=4, 64 Q heads / 8 KV heads -> 16 Q heads per rank.
+  independent.  Example: cp=4, 64 Q heads / 8 KV heads -> 16 Q heads per rank.  The backward
+  pass runs the same exchanges in reverse; the guide above (section 2.3, gradient handling)
+  reduce-scatters the gradients of the split sequence.  ``backward.py`` writes out the chain
+  rule of the attention definition, whole and per KV chunk.
 
 Pins (what the oracle is checked against, in ``tests/test_oracle_pins.py``): pure-Python
 brute force on tiny inputs (softmax computed without max-subtraction, and the FCP article's
 blockwise online accumulation with shuffled block order), closed forms (Q = 0, constant V,
-causal row 0, K = 0), a library special case (``torch.nn.functional.scaled_dot_product_attention``
+causal row 0, K = 0), central finite differences of the brute-force forward for the gradients,
+the sum over chunks of the per-chunk gradients, a library special case (``torch.nn.functional.scaled_dot_product_attention``
 in float64), merge invariants (permutation, associativity) and the worked layout examples the
 pages print (``tests/golden/``).  Planted-mistake tests show each pin family fails on a
 plausible bug.
@@ -35,6 +39,7 @@ plausible bug.
 
 from .layouts import shard_positions, sub_chunk_positions, visible_pair_count
 from .attention import attention, merge
+from .backward import attention_backward, chunk_backward
 from .ulysses import seq_to_head, head_to_seq
 
 __all__ = [
@@ -43,6 +48,8 @@ __all__ = [
     "visible_pair_count",
     "attention",
     "merge",
+    "attention_backward",
+    "chunk_backward",
     "seq_to_head",
     "head_to_seq",
 ]

@@ -14,7 +14,10 @@ Pins used:
   * a library special case: torch.nn.functional.scaled_dot_product_attention in float64, with
     GQA expressed through torch.repeat_interleave of the KV heads, and torch.logsumexp;
   * worked examples printed on the pages (tests/golden/);
-  * merge invariants: any order of partials, associativity, extreme LSE spreads.
+  * merge invariants: any order of partials, associativity, extreme LSE spreads;
+  * gradients: central finite differences of the brute-force forward for every element, torch
+    autograd through SDPA in float64, the sum of per-chunk gradients over a sharded sequence,
+    softmax-Jacobian invariants and closed forms.
 """
 
 import math
@@ -312,5 +315,105 @@ def check_ulysses(orc):
             assert np.array_equal(rt[s], qs[s])
 
 
+# ---------------------------------------------------------------- gradients
+
+def _brute_loss(q, k, v, d_o, qpos, kpos, causal, scale):
+    """sum(dO * O) with O from the pure-Python brute force: its gradient is the backward pass."""
+    o, _ = brute_attention(q.tolist(), k.tolist(), v.tolist(), qpos.tolist(), kpos.tolist(),
+                           causal, scale)
+    return float((np.asarray(o) * d_o).sum())
+
+
+def check_backward_finite_differences(orc):
+    """Every gradient element against a central difference of the brute-force forward."""
+    eps = 1e-6
+    for seed, sq, skv, hq, hkv, d, qp, kp, causal in TINY_CASES[:4]:
+        q, k, v, qpos, kpos = _tiny_case(seed, sq, skv, hq, hkv, d, qp, kp)
+        d_o = np.random.default_rng(seed + 100).standard_normal(q.shape)
+        scale = 1.0 / math.sqrt(d)
+        dq, dk, dv = orc.attention_backward(q, k, v, d_o, qpos, kpos, causal=causal)
+        for name, x, g in (("dQ", q, dq), ("dK", k, dk), ("dV", v, dv)):
+            for idx in np.ndindex(x.shape):
+                xp = x.copy()
+                xm = x.copy()
+                xp[idx] += eps
+                xm[idx] -= eps
+                args_p = [xp if y is x else y for y in (q, k, v)]
+                args_m = [xm if y is x else y for y in (q, k, v)]
+                fd = (_brute_loss(*args_p, d_o, qpos, kpos, causal, scale) -
+                      _brute_loss(*args_m, d_o, qpos, kpos, causal, scale)) / (2 * eps)
+                assert abs(fd - g[idx]) < 1e-7, f"{name}{idx} differs from finite differences (case {seed})"
+
+
+def check_backward_autograd(orc):
+    """torch autograd through SDPA in float64 (GQA via repeat_interleave, which sums the
+    group's gradients back onto each KV head)."""
+    rng = np.random.default_rng(9)
+    for causal in (False, True):
+        s, hq, hkv, d = 20, 6, 2, 8
+        q = rng.standard_normal((s, hq, d))
+        k = rng.standard_normal((s, hkv, d))
+        v = rng.standard_normal((s, hkv, d))
+        d_o = rng.standard_normal((s, hq, d))
+        pos = np.arange(s)
+        dq, dk, dv = orc.attention_backward(q, k, v, d_o, pos, pos, causal=causal)
+        tq = torch.from_numpy(q).requires_grad_()
+        tk = torch.from_numpy(k).requires_grad_()
+        tv = torch.from_numpy(v).requires_grad_()
+        g = hq // hkv
+        out = torch.nn.functional.scaled_dot_product_attention(
+            tq.permute(1, 0, 2)[None], tk.permute(1, 0, 2).repeat_interleave(g, dim=0)[None],
+            tv.permute(1, 0, 2).repeat_interleave(g, dim=0)[None], is_causal=causal)
+        out[0].permute(1, 0, 2).backward(torch.from_numpy(d_o))
+        assert np.allclose(dq, tq.grad.numpy(), atol=1e-11), "dQ differs from autograd"
+        assert np.allclose(dk, tk.grad.numpy(), atol=1e-11), "dK differs from autograd"
+        assert np.allclose(dv, tv.grad.numpy(), atol=1e-11), "dV differs from autograd"
+
+
+def check_backward_chunks(orc):
+    """Per-chunk gradients (against the final O and LSE) add up to the unsharded gradients, in
+    any chunk order; closed forms and invariants of the softmax Jacobian."""
+    rng = np.random.default_rng(13)
+    seq, cp, hq, hkv, d = 32, 4, 4, 2, 6
+    q = rng.standard_normal((seq, hq, d))
+    k = rng.standard_normal((seq, hkv, d))
+    v = rng.standard_normal((seq, hkv, d))
+    d_o = rng.standard_normal((seq, hq, d))
+    full = np.arange(seq)
+    dq_ref, dk_ref, dv_ref = orc.attention_backward(q, k, v, d_o, full, full, causal=True)
+    # the gradients do not depend on how the sequence is sharded (strided query shards here,
+    # contiguous KV chunks), chunk order shuffled
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    o_all, lse_all = orc.attention(q, k, v, full, full, causal=True)
+    for r in range(cp):
+        qpos = np.arange(r, seq, cp)
+        order = rng.permutation(cp)
+        for c in order:
+            kpos = np.arange(c * seq // cp, (c + 1) * seq // cp)
+            a, b, e = orc.chunk_backward(q[qpos], k[kpos], v[kpos], d_o[qpos], o_all[qpos],
+                                         lse_all[qpos], qpos, kpos, causal=True)
+            dq[qpos] += a
+            dk[kpos] += b  # the reduce-scatter: each chunk's owner sums every rank's share
+            dv[kpos] += e
+    assert np.allclose(dq, dq_ref, atol=1e-12), "chunked dQ differs from the unsharded gradient"
+    assert np.allclose(dk, dk_ref, atol=1e-12), "chunked dK differs"
+    assert np.allclose(dv, dv_ref, atol=1e-12), "chunked dV differs"
+    # invariants: each row's dS sums to 0, so the dK of every KV head sums to 0 over keys; each
+    # row's P sums to 1, so the dV of every KV head sums to its group's dO
+    assert np.allclose(dk_ref.sum(axis=0), 0.0, atol=1e-12)
+    for g in range(hkv):
+        grp = d_o[:, g * (hq // hkv):(g + 1) * (hq // hkv), :].sum(axis=(0, 1))
+        assert np.allclose(dv_ref[:, g].sum(axis=0), grp, atol=1e-12)
+    # constant V: O does not depend on Q or K at all
+    vc = np.broadcast_to(rng.standard_normal(d), v.shape).copy()
+    a, b, _ = orc.attention_backward(q, k, vc, d_o, full, full, causal=True)
+    assert np.allclose(a, 0.0, atol=1e-12) and np.allclose(b, 0.0, atol=1e-12)
+    # causal row 0 sees one key: its softmax is the constant 1, so its dQ is 0
+    assert np.allclose(dq_ref[0], 0.0, atol=1e-12)
+
+
 ALL_CHECKS = [check_brute_force, check_fcp_blockwise, check_closed_forms, check_sdpa,
-              check_merge, check_layouts, check_ulysses]
+              check_merge, check_layouts, check_ulysses, check_backward_finite_differences,
+              check_backward_autograd, check_backward_chunks]

@@ -35,7 +35,7 @@ def _load(name, replace=None):
 
 def _mutant(file, old, new):
     mods = {n: _load(n, (old, new) if n == file else None)
-            for n in ("attention", "layouts", "ulysses")}
+            for n in ("attention", "layouts", "ulysses", "backward")}
     ns = types.SimpleNamespace()
     for n in ("attention", "merge"):
         setattr(ns, n, getattr(mods["attention"], n))
@@ -43,6 +43,8 @@ def _mutant(file, old, new):
         setattr(ns, n, getattr(mods["layouts"], n))
     for n in ("seq_to_head", "head_to_seq"):
         setattr(ns, n, getattr(mods["ulysses"], n))
+    for n in ("attention_backward", "chunk_backward"):
+        setattr(ns, n, getattr(mods["backward"], n))
     return ns
 
 
@@ -69,6 +71,19 @@ MUTANTS = [
     ("visible_strict", "layouts", 'side="right"', 'side="left"'),
     ("two_block_mirror", "layouts", "late = [(2 * cp - 1 - rank) * block + i",
      "late = [(cp + rank) * block + i"),
+    ("bwd_no_softmax_jacobian_term", "backward",
+     "ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))", "ds = p * dp"),
+    ("bwd_dq_unscaled", "backward", "dq[:, h, :] = scale * (ds @ k[:, g, :])",
+     "dq[:, h, :] = (ds @ k[:, g, :])"),
+    ("bwd_dk_uses_p", "backward", "dk[:, g, :] += scale * (ds.T @ q[:, h, :])",
+     "dk[:, g, :] += scale * (p.T @ q[:, h, :])"),
+    ("bwd_gqa_overwrite", "backward", "dv[:, g, :] += p.T @ d_o[:, h, :]",
+     "dv[:, g, :] = p.T @ d_o[:, h, :]"),
+    ("bwd_dv_uses_v", "backward", "dp = d_o[:, h, :] @ v[:, g, :].T", "dp = d_o[:, h, :] @ k[:, g, :].T"),
+    ("chunk_delta_from_chunk_only", "backward", "ds = p * (dp - delta[:, h][:, None])",
+     "ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))"),
+    ("chunk_lse_ignored", "backward",
+     "p = np.exp(s - np.where(finite, lse[:, h], 0.0)[:, None])", "p = np.exp(s)"),
     ("ulysses_interleaved_q_heads", "ulysses",
      "out[r][np.asarray(positions[s])] = x_shards[s][:, r * hl:(r + 1) * hl, :]",
      "out[r][np.asarray(positions[s])] = x_shards[s][:, r::cp, :]"),
