@@ -15,6 +15,9 @@ from .api import (  # noqa: F401
     partial_attn,
     partial_attn_chunks,
     merge_partials,
+    attn_bwd_prep,
+    partial_attn_bwd,
+    bwd_aux_floats,
     ulysses_reshard,
     library_path,
     load_library,
@@ -32,6 +35,9 @@ __all__ = [
     "partial_attn",
     "partial_attn_chunks",
     "merge_partials",
+    "attn_bwd_prep",
+    "partial_attn_bwd",
+    "bwd_aux_floats",
     "ulysses_reshard",
     "library_path",
     "load_library",

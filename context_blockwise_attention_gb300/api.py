@@ -51,6 +51,18 @@ class _AttnDesc(ctypes.Structure):
     ]
 
 
+class _AttnBwdDesc(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("d_o", ctypes.c_void_p), ("in_dtype", ctypes.c_int32), ("flags", ctypes.c_int32),
+        ("aux", ctypes.c_void_p), ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p),
+        ("dv", ctypes.c_void_p), ("sq", ctypes.c_int64), ("skv", ctypes.c_int64),
+        ("hq", ctypes.c_int32), ("hkv", ctypes.c_int32), ("d", ctypes.c_int32),
+        ("causal", ctypes.c_int32), ("scale", ctypes.c_float), ("wait_timeout_ms", ctypes.c_int32),
+        ("q_pos", _PosMap), ("kv_pos", _PosMap), ("status", ctypes.c_void_p),
+    ]
+
+
 class _KvChunk(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("skv", ctypes.c_int64),
                 ("kv_pos", _PosMap)]
@@ -93,6 +105,10 @@ def load_library():
     lib.cp_partial_attn.argtypes = [ctypes.POINTER(_AttnDesc), vp]
     lib.cp_partial_attn_chunks.restype = i32
     lib.cp_partial_attn_chunks.argtypes = [ctypes.POINTER(_AttnDesc), i32, ctypes.POINTER(_KvChunk), vp]
+    lib.cp_attn_bwd_prep.restype = i32
+    lib.cp_attn_bwd_prep.argtypes = [vp, i32, vp, i32, vp, i64, i32, i32, vp, vp]
+    lib.cp_partial_attn_bwd.restype = i32
+    lib.cp_partial_attn_bwd.argtypes = [ctypes.POINTER(_AttnBwdDesc), vp]
     lib.cp_merge_partials.restype = i32
     lib.cp_merge_partials.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), i64, i32, i32,
                                       vp, i32, vp, vp]
@@ -279,6 +295,75 @@ def partial_attn_chunks(q, chunks, q_pos: PosMap, causal=True, scale=0.0, o=None
     desc.wait_timeout_ms = int(wait_timeout_ms)
     _check(lib.cp_partial_attn_chunks(ctypes.byref(desc), n, arr, _stream(stream)))
     return o, lse
+
+
+def bwd_aux_floats(sq, hq):
+    """Size of the per-row backward workspace (``CP_BWD_AUX_FLOATS``)."""
+    return 2 * int(hq) * ((int(sq) + 127) // 128 * 128)
+
+
+def attn_bwd_prep(o, d_o, lse, aux=None, stream=None):
+    """Per-row quantities of the backward pass of a query shard from its final ``o`` and ``lse``
+    and the output gradient ``d_o`` (all [Sq, Hq, D] / [Sq, Hq]); returns the fp32 workspace."""
+    lib = load_library()
+    for t, n in ((o, "o"), (d_o, "d_o"), (lse, "lse")):
+        _need_cuda(t, n)
+    if o.dim() != 3 or d_o.shape != o.shape or tuple(lse.shape) != tuple(o.shape[:2]):
+        raise CpError(CP_ERR_INVALID_ARG, "o and d_o must be [Sq, Hq, D], lse [Sq, Hq]")
+    if lse.dtype != torch.float32:
+        raise CpError(CP_ERR_INVALID_ARG, "lse must be fp32")
+    sq, hq, d = o.shape
+    if aux is None:
+        aux = torch.empty(bwd_aux_floats(sq, hq), dtype=torch.float32, device=o.device)
+    _need_cuda(aux, "aux")
+    if aux.dtype != torch.float32 or aux.numel() < bwd_aux_floats(sq, hq):
+        raise CpError(CP_ERR_INVALID_ARG, "aux must be fp32 with bwd_aux_floats(sq, hq) elements")
+    _check(lib.cp_attn_bwd_prep(ctypes.c_void_p(o.data_ptr()), _dtype_code(o.dtype),
+                                ctypes.c_void_p(d_o.data_ptr()), _dtype_code(d_o.dtype),
+                                ctypes.c_void_p(lse.data_ptr()), sq, hq, d,
+                                ctypes.c_void_p(aux.data_ptr()), _stream(stream)))
+    return aux
+
+
+def partial_attn_bwd(q, k, v, d_o, aux, q_pos: PosMap, kv_pos: PosMap, dq, dk, dv, causal=True,
+                     scale=0.0, status=None, wait_timeout_ms=0, stream=None):
+    """Adds one (query shard, KV chunk) pair's share of the attention gradients into ``dq``
+    [Sq, Hq, D] and ``dk``, ``dv`` [Skv, Hkv, D] (fp32, accumulated in place)."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (d_o, "d_o"), (aux, "aux"), (dq, "dq"), (dk, "dk"),
+                 (dv, "dv")):
+        _need_cuda(t, n)
+    if q.dim() != 3 or k.dim() != 3 or v.shape != k.shape or d_o.shape != q.shape:
+        raise CpError(CP_ERR_INVALID_ARG, "q, d_o must be [Sq, Hq, D]; k and v [Skv, Hkv, D]")
+    if not (q.dtype == k.dtype == v.dtype == d_o.dtype):
+        raise CpError(CP_ERR_INVALID_ARG, "q, k, v, d_o must share a dtype")
+    sq, hq, d = q.shape
+    skv, hkv, dk_ = k.shape
+    if dk_ != d:
+        raise CpError(CP_ERR_INVALID_ARG, "head_dim mismatch")
+    if dq.shape != q.shape or dk.shape != k.shape or dv.shape != k.shape or \
+            any(t.dtype != torch.float32 for t in (dq, dk, dv, aux)):
+        raise CpError(CP_ERR_INVALID_ARG, "dq, dk, dv must be fp32 and shaped like q, k, v")
+    if aux.numel() < bwd_aux_floats(sq, hq):
+        raise CpError(CP_ERR_INVALID_ARG, "aux is smaller than bwd_aux_floats(sq, hq)")
+    desc = _AttnBwdDesc()
+    desc.q, desc.k, desc.v, desc.d_o = q.data_ptr(), k.data_ptr(), v.data_ptr(), d_o.data_ptr()
+    desc.in_dtype = _dtype_code(q.dtype)
+    desc.aux = aux.data_ptr()
+    desc.dq, desc.dk, desc.dv = dq.data_ptr(), dk.data_ptr(), dv.data_ptr()
+    desc.sq, desc.skv, desc.hq, desc.hkv, desc.d = sq, skv, hq, hkv, d
+    desc.causal = 1 if causal else 0
+    desc.scale = float(scale)
+    desc.q_pos = _PosMap(q_pos.base, q_pos.stride)
+    desc.kv_pos = _PosMap(kv_pos.base, kv_pos.stride)
+    if status is not None:
+        _need_cuda(status, "status")
+        if status.dtype != torch.int32:
+            raise CpError(CP_ERR_INVALID_ARG, "status must be int32")
+        desc.status = status.data_ptr()
+    desc.wait_timeout_ms = int(wait_timeout_ms)
+    _check(lib.cp_partial_attn_bwd(ctypes.byref(desc), _stream(stream)))
+    return dq, dk, dv
 
 
 def merge_partials(o_parts, lse_parts, out_dtype=torch.bfloat16, o=None, lse=None, stream=None):

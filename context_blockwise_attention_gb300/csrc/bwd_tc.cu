@@ -1,0 +1,630 @@
+// Backward of one (query shard, KV chunk) partial for bf16 inputs on the tcgen05 tensor cores.
+//
+// What it computes: the chain rule of the partial attention ("PCP and DCP sequence parallelism
+// guide", section 2.3: in training the split sequence's gradients are reduce-scattered across
+// ranks; this is one rank's share for one chunk).  Per head, against the rows' final LSE and
+// D = dO . O (prep kernel):
+//   S^T  = K Q^T                 P^T  = 2^(scale*log2(e) S^T - LSE*log2(e))   (keys x queries)
+//   dP^T = V dO^T                dS^T = P^T o (dP^T - D)
+//   dV  += P^T dO                dK  += scale dS^T Q                dQ += scale dS K
+//
+// How (GB300 design):
+//   * Persistent, one CTA per SM.  A unit is one 128-key KV tile of one Q head; it walks every
+//     128-row query tile that can see the KV tile (causal: tiles whose last row's position is at
+//     least the tile's first key position).  Units are numbered earliest keys first (they see
+//     the most query tiles) and dealt round by round in snake order.
+//   * warp 0: TMA producer (K, V once per unit; Q, dO tiles and the rows' -LSE*log2(e), -D runs
+//     per query tile).  warp 1: allocates tensor memory, issues tcgen05.mma (whole warp waits,
+//     one elected lane issues).  warps 4-7: gradient warpgroup, one thread per key row -- turns
+//     S^T into P^T and dP^T into dS^T.  warps 8-11: reduction warpgroup -- adds dQ (per query
+//     tile) and dK, dV (per unit) into global memory with TMA bulk reductions (fp32 add), so
+//     concurrent CTAs and GQA heads accumulate without a separate pass.
+//   * Tensor memory: S^T (128 fp32 columns, P^T bf16 written over its first 64), dP^T (128,
+//     dS^T bf16 over its first 64), dV and dK accumulators (D each), dQ (D; for D = 128 it
+//     reuses the S^T columns once the dV product has consumed P^T).
+//   * The five products: S^T and dP^T are K-major x K-major from shared memory; dV and dK take
+//     P^T / dS^T straight from tensor memory with dO / Q as MN-major B operands; dQ takes dS from
+//     shared memory as an MN-major A operand (the gradient warps write it there in the 128-byte
+//     swizzled layout a TMA load would produce) and K as MN-major B.
+//   * Every mbarrier wait is bounded by %globaltimer; see sync.cuh.
+#include <math.h>
+#include <string.h>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "sync.cuh"
+
+namespace cpattn {
+
+namespace {
+
+constexpr int kRows = 128;     // query rows per tile
+constexpr int kKeys = 128;     // keys per KV tile
+constexpr int kThreads = 384;  // 12 warps
+
+enum BwdSite : int {
+  kSKvFull = 1,
+  kSKvEmpty = 2,
+  kSQFull = 3,
+  kSQEmpty = 4,
+  kSSFull = 5,
+  kSPReady = 6,
+  kSDpFull = 7,
+  kSDsReady = 8,
+  kSDqFull = 9,
+  kSDqFree = 10,
+  kSAccFull = 11,
+  kSAccEmpty = 12,
+};
+
+struct BwdParams {
+  int32_t* status;
+  const float* aux;  // [2][hq][sq_pad]: -LSE*log2(e), -D
+  int64_t sq, skv, sq_pad;
+  int32_t hq, hkv, group, causal;
+  int32_t n_qt, n_kt;  // query tiles, KV tiles
+  int64_t n_units;     // n_kt * hq
+  float scale, sl2;    // scale, scale * log2(e)
+  int64_t q_base, q_stride, k_base, k_stride;
+  int64_t timeout_ns;
+};
+
+template <int D>
+struct BLayout {
+  static constexpr int kChunkBytes = 128 * 128;     // 128 rows x 128 bytes
+  static constexpr int kTileBytes = kRows * D * 2;  // bf16 [128, D]
+  static constexpr int kChunks = D / 64;
+  static constexpr int kQStages = (D == 64) ? 2 : 1;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kTileBytes;
+  static constexpr int kOffQ = 2 * kTileBytes;
+  static constexpr int kOffDO = kOffQ + kQStages * kTileBytes;
+  static constexpr int kOffDS = kOffDO + kQStages * kTileBytes;  // dS, 128 keys x 128 queries bf16
+  static constexpr int kOffAux = kOffDS + 2 * kChunkBytes;       // per stage: 128 + 128 floats
+  static constexpr int kOffStage = kOffAux + kQStages * 1024;    // 4 warps x 2 x 4 KB
+  static constexpr int kOffBar = kOffStage + 8 * 4096;
+  // kv_full, kv_empty, q_full[S], q_empty[S], s_full, p_ready, dp_full, ds_ready, dq_full,
+  // dq_free, acc_full, acc_empty, drain
+  static constexpr int kNumBars = 2 + 2 * kQStages + 9;
+  static constexpr int kOffCtl = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffCtl + 16;
+  static constexpr int kSmemLaunch = kBytes + 1024;
+  // tensor memory columns
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+  static constexpr uint32_t kColDQ = (D == 64) ? 384 : 0;
+};
+static_assert(BLayout<128>::kSmemLaunch <= 232448, "shared memory budget (D=128)");
+static_assert(BLayout<64>::kSmemLaunch <= 232448, "shared memory budget (D=64)");
+static_assert(BLayout<64>::kColDQ + 64 <= 512 && BLayout<128>::kColDK + 128 <= 512, "tensor memory budget");
+
+// Register split: 4 warps x 120 (TMA / MMA) + 4 x 248 (gradient) + 4 x 136 (reduction) =
+// 12 warps x 168, the launch's allocation.
+constexpr uint32_t kRegsControl = 120;
+constexpr uint32_t kRegsGrad = 248;
+constexpr uint32_t kRegsRed = 136;
+static_assert(4 * kRegsControl + 4 * kRegsGrad + 4 * kRegsRed == 12 * 168, "register split must match launch");
+
+struct Bars {
+  uint32_t kv_full, kv_empty, q_full, q_empty;  // q_*: stage 0, +8 per stage
+  uint32_t s_full, p_ready, dp_full, ds_ready, dq_full, dq_free, acc_full, acc_empty, drain;
+};
+
+struct BUnit {
+  int jt, h, g;
+  int t0;   // first query tile that sees the KV tile
+  int nit;  // query tiles to visit
+};
+
+__device__ __forceinline__ BUnit decode_bunit(const BwdParams& p, int64_t u) {
+  BUnit w;
+  w.jt = static_cast<int>(u / p.hq);
+  w.h = static_cast<int>(u % p.hq);
+  w.g = w.h / p.group;
+  w.t0 = 0;
+  if (p.causal) {
+    const int64_t kp0 = p.k_base + p.k_stride * static_cast<int64_t>(w.jt) * kKeys;
+    int64_t rmin = 0;  // first query row whose position reaches the tile's first key
+    if (kp0 > p.q_base) rmin = (kp0 - p.q_base + p.q_stride - 1) / p.q_stride;
+    w.t0 = rmin >= p.sq ? p.n_qt : static_cast<int>(rmin / kRows);
+  }
+  w.nit = p.n_qt - w.t0;
+  return w;
+}
+
+// One warp's bulk reduction: 32 fp32 columns of its 32 rows, times `mul`, staged in one of its
+// two 4 KB swizzled boxes and added into `tm` at (x, y).  Rows past `rows` are clipped by the
+// tensor map; a box that starts past them is skipped.  Returns the updated reduction count.
+__device__ __forceinline__ uint32_t reduce_box(uint32_t stage0, int lane, uint32_t nred, const uint32_t (&v)[32],
+                                               float mul, const CUtensorMap* tm, int32_t x, int32_t y, int64_t rows) {
+  if (y >= rows) return nred;
+  const uint32_t sb = stage0 + (nred & 1u) * 4096u;
+  if (lane == 0) ptx::bulk_wait_read_1();  // the reduction that used this buffer has read it
+  __syncwarp();
+  const uint32_t row = sb + static_cast<uint32_t>(lane) * 128u;
+  const uint32_t sw = static_cast<uint32_t>(lane & 7);
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    ptx::sts128(row + ((static_cast<uint32_t>(q) ^ sw) << 4), __float_as_uint(__uint_as_float(v[4 * q]) * mul),
+                __float_as_uint(__uint_as_float(v[4 * q + 1]) * mul), __float_as_uint(__uint_as_float(v[4 * q + 2]) * mul),
+                __float_as_uint(__uint_as_float(v[4 * q + 3]) * mul));
+  ptx::fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    ptx::tma_reduce_add_2d(tm, sb, x, y);
+    ptx::bulk_commit();
+  }
+  return nred + 1;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_tc_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dq,
+                       const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv) {
+  using L = BLayout<D>;
+  using namespace sync;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t cta = blockIdx.x;
+  const int64_t grid = gridDim.x;
+
+  Bars b;
+  b.kv_full = sbase + L::kOffBar;
+  b.kv_empty = b.kv_full + 8;
+  b.q_full = b.kv_empty + 8;
+  b.q_empty = b.q_full + 8 * L::kQStages;
+  b.s_full = b.q_empty + 8 * L::kQStages;
+  b.p_ready = b.s_full + 8;
+  b.dp_full = b.p_ready + 8;
+  b.ds_ready = b.dp_full + 8;
+  b.dq_full = b.ds_ready + 8;
+  b.dq_free = b.dq_full + 8;
+  b.acc_full = b.dq_free + 8;
+  b.acc_empty = b.acc_full + 8;
+  b.drain = b.acc_empty + 8;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffCtl);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffCtl + 4);
+  const Ctl ctl{abort_flag, p.status, p.timeout_ns};
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    ptx::mbar_init(b.kv_full, 1);
+    ptx::mbar_init(b.kv_empty, 1);
+    for (int s = 0; s < L::kQStages; ++s) {
+      ptx::mbar_init(b.q_full + 8 * s, 1);
+      ptx::mbar_init(b.q_empty + 8 * s, 1);
+    }
+    ptx::mbar_init(b.s_full, 1);
+    ptx::mbar_init(b.p_ready, 4);
+    ptx::mbar_init(b.dp_full, 1);
+    ptx::mbar_init(b.ds_ready, 4);
+    ptx::mbar_init(b.dq_full, 1);
+    ptx::mbar_init(b.dq_free, 4);
+    ptx::mbar_init(b.acc_full, 1);
+    ptx::mbar_init(b.acc_empty, 4);
+    ptx::mbar_init(b.drain, 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const uint32_t sK = sbase + L::kOffK;
+  const uint32_t sV = sbase + L::kOffV;
+  const uint32_t sQ = sbase + L::kOffQ;
+  const uint32_t sDO = sbase + L::kOffDO;
+  const uint32_t sDS = sbase + L::kOffDS;
+  const uint32_t sAux = sbase + L::kOffAux;
+
+  if (warp < 4) {
+    ptx::regs_dec<kRegsControl>();
+    if (warp == 0) {
+      // ============================================================== TMA producer
+      const bool leader = ptx::elect_one();
+      if (leader) {
+        ptx::tma_prefetch_desc(&tm_q);
+        ptx::tma_prefetch_desc(&tm_do);
+        ptx::tma_prefetch_desc(&tm_k);
+        ptx::tma_prefetch_desc(&tm_v);
+      }
+      int64_t gi = 0, ku = 0;  // query tiles and units with work issued so far
+      bool ok = true;
+      for (int64_t k = 0; ok; ++k) {
+        const int64_t u = unit_of(k, cta, grid);
+        if (u >= p.n_units) break;
+        const BUnit w = decode_bunit(p, u);
+        if (w.nit <= 0) continue;
+        if (ku > 0 && !(ok = wait_warp(b.kv_empty, static_cast<uint32_t>((ku - 1) & 1), ctl, kSKvEmpty))) break;
+        if (leader) {
+          ptx::mbar_arrive_expect_tx(b.kv_full, 2 * L::kTileBytes);
+          for (int cc = 0; cc < L::kChunks; ++cc) {
+            ptx::tma_load_2d(sK + cc * L::kChunkBytes, &tm_k, w.g * D + cc * 64, w.jt * kKeys, b.kv_full);
+            ptx::tma_load_2d(sV + cc * L::kChunkBytes, &tm_v, w.g * D + cc * 64, w.jt * kKeys, b.kv_full);
+          }
+        }
+        __syncwarp();
+        for (int it = 0; it < w.nit; ++it, ++gi) {
+          const int t = w.t0 + it;
+          const int st = static_cast<int>(gi % L::kQStages);
+          const uint32_t ph = static_cast<uint32_t>((gi / L::kQStages) & 1);
+          if (!(ok = wait_warp(b.q_empty + 8 * st, ph ^ 1, ctl, kSQEmpty))) break;
+          if (leader) {
+            const uint32_t full = b.q_full + 8 * st;
+            ptx::mbar_arrive_expect_tx(full, 2 * L::kTileBytes + 1024);
+            for (int cc = 0; cc < L::kChunks; ++cc) {
+              ptx::tma_load_2d(sQ + st * L::kTileBytes + cc * L::kChunkBytes, &tm_q, w.h * D + cc * 64,
+                               t * kRows, full);
+              ptx::tma_load_2d(sDO + st * L::kTileBytes + cc * L::kChunkBytes, &tm_do, w.h * D + cc * 64,
+                               t * kRows, full);
+            }
+            const float* a0 = p.aux + static_cast<int64_t>(w.h) * p.sq_pad + static_cast<int64_t>(t) * kRows;
+            const float* a1 = p.aux + (static_cast<int64_t>(p.hq) + w.h) * p.sq_pad + static_cast<int64_t>(t) * kRows;
+            ptx::bulk_load(sAux + st * 1024, a0, 512, full);
+            ptx::bulk_load(sAux + st * 1024 + 512, a1, 512, full);
+          }
+          __syncwarp();
+        }
+        ++ku;
+      }
+      if (*abort_flag && leader) {
+        // loads in flight must land before the CTA's shared memory goes away
+        if (ku > 0) wait_drain(b.kv_full, static_cast<uint32_t>((ku - 1) & 1), p.timeout_ns);
+        for (int s = 0; s < L::kQStages; ++s) {
+          const int64_t last = (gi - 1 - s >= 0) ? gi - 1 - ((gi - 1 - s) % L::kQStages) : -1;
+          if (last >= 0)
+            wait_drain(b.q_full + 8 * s, static_cast<uint32_t>((last / L::kQStages) & 1), p.timeout_ns);
+        }
+      }
+      __syncwarp();
+    } else if (warp == 1) {
+      // ============================================================== MMA issuer
+      const bool leader = ptx::elect_one();
+      constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kKeys, kRows, 0, 0);  // S^T, dP^T
+      constexpr uint32_t kIdescG = ptx::idesc_bf16_f32(kKeys, D, 0, 1);      // dV, dK (A in TMEM)
+      constexpr uint32_t kIdescQ = ptx::idesc_bf16_f32(kRows, D, 1, 1);      // dQ (A = dS, MN-major)
+      const uint64_t dK_k = ptx::smem_desc_sw128(sK, 16, 1024);
+      const uint64_t dV_k = ptx::smem_desc_sw128(sV, 16, 1024);
+      const uint64_t dQ_k = ptx::smem_desc_sw128(sQ, 16, 1024);
+      const uint64_t dDO_k = ptx::smem_desc_sw128(sDO, 16, 1024);
+      const uint64_t dQ_mn = ptx::smem_desc_sw128(sQ, L::kChunkBytes, 1024);
+      const uint64_t dDO_mn = ptx::smem_desc_sw128(sDO, L::kChunkBytes, 1024);
+      const uint64_t dK_mn = ptx::smem_desc_sw128(sK, L::kChunkBytes, 1024);
+      const uint64_t dDS_mn = ptx::smem_desc_sw128(sDS, L::kChunkBytes, 1024);
+      constexpr uint64_t kTileUnits = L::kTileBytes >> 4;
+
+      // M=128, N=128, K=D; both operands K-major (rows x D, 64-column swizzled boxes)
+      auto issue_kk = [&](uint32_t d_tmem, uint64_t a0, uint64_t b0) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4);
+          ptx::mma_ss(d_tmem, a0 + off, b0 + off, kIdescS, kk > 0 ? 1u : 0u);
+        }
+      };
+      // M=128 keys, N=D, K=128 queries: A (bf16 packed, 8 columns per 16 queries) in tensor memory
+      auto issue_ts = [&](uint32_t d_tmem, uint32_t a_tmem, uint64_t b_mn, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < kRows / 16; ++kk)
+          ptx::mma_ts(d_tmem, a_tmem + kk * 8, b_mn + static_cast<uint64_t>(kk * 128), kIdescG,
+                      (acc || kk > 0) ? 1u : 0u);
+      };
+      // M=128 queries, N=D, K=128 keys: dS (MN-major) x K (MN-major)
+      auto issue_dq = [&](uint32_t d_tmem) {
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk)
+          ptx::mma_ss(d_tmem, dDS_mn + static_cast<uint64_t>(kk * 128), dK_mn + static_cast<uint64_t>(kk * 128),
+                      kIdescQ, kk > 0 ? 1u : 0u);
+      };
+
+      int64_t gi = 0, ku = 0;
+      bool ok = true;
+      for (int64_t k = 0; ok; ++k) {
+        const int64_t u = unit_of(k, cta, grid);
+        if (u >= p.n_units) break;
+        const BUnit w = decode_bunit(p, u);
+        if (w.nit <= 0) continue;
+        if (!(ok = wait_warp(b.kv_full, static_cast<uint32_t>(ku & 1), ctl, kSKvFull))) break;
+        for (int it = 0; it < w.nit; ++it, ++gi) {
+          const bool first = (it == 0);
+          const int st = static_cast<int>(gi % L::kQStages);
+          const uint32_t ph = static_cast<uint32_t>((gi / L::kQStages) & 1);
+          const uint32_t prev = static_cast<uint32_t>((gi - 1) & 1);
+          const uint32_t cur = static_cast<uint32_t>(gi & 1);
+          if (!(ok = wait_warp(b.q_full + 8 * st, ph, ctl, kSQFull))) break;
+          // D = 128: the previous dQ sits in the S^T columns until the reduction warps read it
+          if (D == 128 && gi > 0 && !(ok = wait_warp(b.dq_free, prev, ctl, kSDqFree))) break;
+          ptx::tc_fence_after();
+          if (leader) {
+            issue_kk(tmem + L::kColS, dK_k, dQ_k + st * kTileUnits);
+            ptx::mma_commit(b.s_full);
+            issue_kk(tmem + L::kColDP, dV_k, dDO_k + st * kTileUnits);
+            ptx::mma_commit(b.dp_full);
+          }
+          __syncwarp();
+          if (!(ok = wait_warp(b.p_ready, cur, ctl, kSPReady))) break;
+          // the unit's first dV overwrites the accumulators: the previous unit's must be read out
+          if (first && ku > 0 && !(ok = wait_warp(b.acc_empty, static_cast<uint32_t>((ku - 1) & 1), ctl, kSAccEmpty)))
+            break;
+          ptx::tc_fence_after();
+          if (leader) issue_ts(tmem + L::kColDV, tmem + L::kColS, dDO_mn + st * kTileUnits, !first);
+          __syncwarp();
+          if (!(ok = wait_warp(b.ds_ready, cur, ctl, kSDsReady))) break;
+          ptx::tc_fence_after();
+          if (leader) issue_ts(tmem + L::kColDK, tmem + L::kColDP, dQ_mn + st * kTileUnits, !first);
+          __syncwarp();
+          if (D == 64 && gi > 0 && !(ok = wait_warp(b.dq_free, prev, ctl, kSDqFree))) break;
+          ptx::tc_fence_after();
+          if (leader) {
+            issue_dq(tmem + L::kColDQ);
+            ptx::mma_commit(b.dq_full);
+            ptx::mma_commit(b.q_empty + 8 * st);
+            if (it == w.nit - 1) {
+              ptx::mma_commit(b.acc_full);
+              ptx::mma_commit(b.kv_empty);
+            }
+          }
+          __syncwarp();
+        }
+        ++ku;
+      }
+      if (!ok) {
+        if (leader) {
+          ptx::mma_commit(b.drain);
+          wait_drain(b.drain, 0, p.timeout_ns);
+        }
+        __syncwarp();
+      }
+    }
+  } else if (warp < 8) {
+    ptx::regs_inc<kRegsGrad>();
+    // ================================================================ gradient warpgroup
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;  // key row inside the KV tile
+    const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + L::kColS + lane_bits;
+    const uint32_t tDP = tmem + L::kColDP + lane_bits;
+    const uint64_t sl2x2 = ptx::f2_pack(p.sl2, p.sl2);
+    const uint32_t ds_row = sDS + static_cast<uint32_t>(r) * 128u;
+    const uint32_t sw = static_cast<uint32_t>(r & 7);
+    int64_t gi = 0;
+    bool ok = true;
+    for (int64_t k = 0; ok; ++k) {
+      const int64_t u = unit_of(k, cta, grid);
+      if (u >= p.n_units) break;
+      const BUnit w = decode_bunit(p, u);
+      if (w.nit <= 0) continue;
+      const int64_t key = static_cast<int64_t>(w.jt) * kKeys + r;
+      const int64_t kpos = p.k_base + p.k_stride * key;
+      int64_t rmin_k = 0;  // first query row that sees this key
+      if (p.causal && kpos > p.q_base) rmin_k = (kpos - p.q_base + p.q_stride - 1) / p.q_stride;
+      // rows past the chunk's end (zero-filled K, V) get P = 0 too: against a very negative LSE
+      // their exponent could overflow, and 0 * inf would reach dQ
+      if (key >= p.skv) rmin_k = INT64_MAX / 2;
+      for (int it = 0; it < w.nit; ++it, ++gi) {
+        const int t = w.t0 + it;
+        const int st = static_cast<int>(gi % L::kQStages);
+        const uint32_t cur = static_cast<uint32_t>(gi & 1);
+        int cmin = 0;  // query columns below cmin do not see this key
+        if (p.causal || key >= p.skv) {
+          const int64_t c = rmin_k - static_cast<int64_t>(t) * kRows;
+          cmin = c <= 0 ? 0 : (c >= kRows ? kRows : static_cast<int>(c));
+        }
+        const uint32_t a_nl = sAux + st * 1024;  // -LSE*log2(e) of the tile's 128 rows
+        const uint32_t a_nd = a_nl + 512;        // -D
+        // the per-row runs were copied by the bulk engine: observe their barrier directly
+        if (!(ok = wait_warp(b.q_full + 8 * st, static_cast<uint32_t>((gi / L::kQStages) & 1), ctl, kSQFull))) break;
+        if (!(ok = wait_warp(b.s_full, cur, ctl, kSSFull))) break;
+        ptx::tc_fence_after();
+        float pf[kRows];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sr[32];
+          ptx::tmem_ld32(tS + c * 32, sr);
+          ptx::tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 nl = ptx::lds128(a_nl + (c * 32 + e4 * 4) * 4);
+            const uint64_t x01 = ptx::f2_fma(
+                ptx::f2_pack(__uint_as_float(sr[4 * e4]), __uint_as_float(sr[4 * e4 + 1])), sl2x2,
+                ptx::f2_pack(nl.x, nl.y));
+            const uint64_t x23 = ptx::f2_fma(
+                ptx::f2_pack(__uint_as_float(sr[4 * e4 + 2]), __uint_as_float(sr[4 * e4 + 3])), sl2x2,
+                ptx::f2_pack(nl.z, nl.w));
+            float x0, x1, x2, x3;
+            ptx::f2_unpack(x01, x0, x1);
+            ptx::f2_unpack(x23, x2, x3);
+            const int col = c * 32 + e4 * 4;
+            pf[col] = ptx::ex2(x0);
+            pf[col + 1] = ptx::ex2(x1);
+            pf[col + 2] = ptx::ex2(x2);
+            pf[col + 3] = ptx::ex2(x3);
+          }
+          if (cmin > c * 32) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (c * 32 + e < cmin) pf[c * 32 + e] = 0.0f;
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) pk[e] = ptx::pack_bf16x2(pf[c * 32 + 2 * e], pf[c * 32 + 2 * e + 1]);
+          ptx::tmem_st16(tS + c * 16, pk);
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(b.p_ready);
+
+        if (!(ok = wait_warp(b.dp_full, cur, ctl, kSDpFull))) break;
+        // the dS buffer in shared memory is free once the previous dQ product has read it
+        if (gi > 0 && !(ok = wait_warp(b.dq_full, static_cast<uint32_t>((gi - 1) & 1), ctl, kSDqFull))) break;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t dr[32];
+          ptx::tmem_ld32(tDP + c * 32, dr);
+          ptx::tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const int col = c * 32 + e4 * 4;
+            const float4 nd = ptx::lds128(a_nd + col * 4);
+            const uint64_t t01 = ptx::f2_add(ptx::f2_pack(__uint_as_float(dr[4 * e4]), __uint_as_float(dr[4 * e4 + 1])),
+                                             ptx::f2_pack(nd.x, nd.y));
+            const uint64_t t23 = ptx::f2_add(
+                ptx::f2_pack(__uint_as_float(dr[4 * e4 + 2]), __uint_as_float(dr[4 * e4 + 3])), ptx::f2_pack(nd.z, nd.w));
+            const uint64_t d01 = ptx::f2_mul(ptx::f2_pack(pf[col], pf[col + 1]), t01);
+            const uint64_t d23 = ptx::f2_mul(ptx::f2_pack(pf[col + 2], pf[col + 3]), t23);
+            float s0, s1, s2, s3;
+            ptx::f2_unpack(d01, s0, s1);
+            ptx::f2_unpack(d23, s2, s3);
+            pk[2 * e4] = ptx::pack_bf16x2(s0, s1);
+            pk[2 * e4 + 1] = ptx::pack_bf16x2(s2, s3);
+          }
+          ptx::tmem_st16(tDP + c * 16, pk);
+          // dS row r, queries c*32 .. c*32+31: four 16-byte chunks of the 64-query box c/2
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t q8 = static_cast<uint32_t>((c & 1) * 4 + i);
+            ptx::sts128(ds_row + static_cast<uint32_t>(c >> 1) * L::kChunkBytes + ((q8 ^ sw) << 4), pk[4 * i],
+                        pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+        ptx::tmem_wait_st();
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(b.ds_ready);
+      }
+    }
+  } else {
+    ptx::regs_dec<kRegsRed>();  // below the launch allocation: give registers back
+    // ================================================================ reduction warpgroup
+    const int wq = warp & 3;
+    const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t stage0 = sbase + L::kOffStage + static_cast<uint32_t>(wq) * 2u * 4096u;
+    int64_t gi = 0, ku = 0;
+    uint32_t nred = 0;  // bulk reductions issued by this warp (staging double buffer)
+    bool ok = true;
+
+    for (int64_t k = 0; ok; ++k) {
+      const int64_t u = unit_of(k, cta, grid);
+      if (u >= p.n_units) break;
+      const BUnit w = decode_bunit(p, u);
+      if (w.nit <= 0) continue;
+      for (int it = 0; it < w.nit; ++it, ++gi) {
+        const int t = w.t0 + it;
+        if (!(ok = wait_warp(b.dq_full, static_cast<uint32_t>(gi & 1), ctl, kSDqFull))) break;
+        ptx::tc_fence_after();
+        // 64 columns at a time (registers); the tensor memory is released after the last read
+#pragma unroll
+        for (int c2 = 0; c2 < D / 64; ++c2) {
+          uint32_t v0[32], v1[32];
+          ptx::tmem_ld32(tmem + L::kColDQ + lane_bits + c2 * 64, v0);
+          ptx::tmem_ld32(tmem + L::kColDQ + lane_bits + c2 * 64 + 32, v1);
+          ptx::tmem_wait_ld();
+          if (c2 == D / 64 - 1) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(b.dq_free);
+          }
+          nred = reduce_box(stage0, lane, nred, v0, p.scale, &tm_dq, w.h * D + c2 * 64, t * kRows + wq * 32, p.sq);
+          nred = reduce_box(stage0, lane, nred, v1, p.scale, &tm_dq, w.h * D + c2 * 64 + 32, t * kRows + wq * 32,
+                            p.sq);
+        }
+      }
+      if (!ok) break;
+      // end of the unit: dK (scaled) and dV
+      if (!(ok = wait_warp(b.acc_full, static_cast<uint32_t>(ku & 1), ctl, kSAccFull))) break;
+      ptx::tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        ptx::tmem_ld32(tmem + L::kColDK + lane_bits + c * 32, v);
+        ptx::tmem_wait_ld();
+        nred = reduce_box(stage0, lane, nred, v, p.scale, &tm_dk, w.g * D + c * 32, w.jt * kKeys + wq * 32, p.skv);
+      }
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        ptx::tmem_ld32(tmem + L::kColDV + lane_bits + c * 32, v);
+        ptx::tmem_wait_ld();
+        nred = reduce_box(stage0, lane, nred, v, 1.0f, &tm_dv, w.g * D + c * 32, w.jt * kKeys + wq * 32, p.skv);
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(b.acc_empty);
+      ++ku;
+    }
+    if (lane == 0) ptx::bulk_wait_all();  // every reduction has completed
+    __syncwarp();
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cp_status launch_bwd_d(const BwdParams& p, const cp_attn_bwd_desc& d, int64_t grid, cudaStream_t s) {
+  CUtensorMap mq, mdo, mk, mv, mdq, mdk, mdv;
+  const int64_t qe = int64_t(d.hq) * D, ke = int64_t(d.hkv) * D;
+  if (!encode_map_2d(&mq, d.q, d.sq, qe, false, 128) || !encode_map_2d(&mdo, d.d_o, d.sq, qe, false, 128) ||
+      !encode_map_2d(&mk, d.k, d.skv, ke, false, 128) || !encode_map_2d(&mv, d.v, d.skv, ke, false, 128) ||
+      !encode_map_2d(&mdq, d.dq, d.sq, qe, true, 32) || !encode_map_2d(&mdk, d.dk, d.skv, ke, true, 32) ||
+      !encode_map_2d(&mdv, d.dv, d.skv, ke, true, 32)) {
+    set_error("cuTensorMapEncodeTiled failed (or the driver entry point is unavailable)");
+    return CP_ERR_CUDA;
+  }
+  constexpr int smem = BLayout<D>::kSmemLaunch;
+  cudaError_t e = cudaFuncSetAttribute(attn_bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attn_bwd_tc_kernel)");
+  attn_bwd_tc_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p, mq, mdo, mk, mv, mdq, mdk, mdv);
+  e = cudaGetLastError();
+  return e == cudaSuccess ? CP_OK : cuda_fail(e, "attn_bwd_tc_kernel launch");
+}
+
+}  // namespace
+
+cp_status launch_partial_attn_bwd_tc(const cp_attn_bwd_desc& d, float scale, int64_t timeout_ns, int num_sms,
+                                     cudaStream_t s) {
+  BwdParams p;
+  p.status = d.status;
+  p.aux = d.aux;
+  p.sq = d.sq;
+  p.skv = d.skv;
+  p.sq_pad = (d.sq + 127) / 128 * 128;
+  p.hq = d.hq;
+  p.hkv = d.hkv;
+  p.group = d.hq / d.hkv;
+  p.causal = d.causal;
+  p.n_qt = static_cast<int32_t>((d.sq + kRows - 1) / kRows);
+  p.n_kt = static_cast<int32_t>((d.skv + kKeys - 1) / kKeys);
+  p.n_units = static_cast<int64_t>(p.n_kt) * d.hq;
+  p.scale = scale;
+  p.sl2 = scale * 1.4426950408889634f;
+  p.q_base = d.q_pos.base;
+  p.q_stride = d.q_pos.stride;
+  p.k_base = d.kv_pos.base;
+  p.k_stride = d.kv_pos.stride;
+  p.timeout_ns = timeout_ns;
+  const int64_t grid = p.n_units < num_sms ? p.n_units : num_sms;
+  if (d.d == 64) return launch_bwd_d<64>(p, d, grid, s);
+  return launch_bwd_d<128>(p, d, grid, s);
+}
+
+}  // namespace cpattn

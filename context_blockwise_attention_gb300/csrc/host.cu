@@ -263,6 +263,64 @@ CP_API cp_status cp_partial_attn_chunks(const cp_attn_desc* desc, int32_t n_chun
   return run_partial(*desc, chunks, n_chunks, stream);
 }
 
+CP_API cp_status cp_attn_bwd_prep(const void* o, int32_t o_dtype, const void* d_o, int32_t do_dtype,
+                                  const float* lse, int64_t sq, int32_t hq, int32_t d, float* aux,
+                                  cudaStream_t stream) {
+  clear_error();
+  if (o_dtype != CP_F32 && o_dtype != CP_BF16) CP_INVALID("cp_attn_bwd_prep: bad o_dtype %d", o_dtype);
+  if (do_dtype != CP_F32 && do_dtype != CP_BF16) CP_INVALID("cp_attn_bwd_prep: bad do_dtype %d", do_dtype);
+  if (sq < 0 || sq > (int64_t(1) << 31) - 256) CP_INVALID("cp_attn_bwd_prep: sq out of range");
+  if (hq <= 0) CP_INVALID("cp_attn_bwd_prep: hq must be positive");
+  if (d != 64 && d != 128) CP_INVALID("cp_attn_bwd_prep: head_dim %d not in {64, 128}", d);
+  if (sq == 0) return CP_OK;
+  if (o == nullptr || d_o == nullptr || lse == nullptr || aux == nullptr)
+    CP_INVALID("cp_attn_bwd_prep: o, d_o, lse and aux must not be NULL");
+  if (!aligned16(o) || !aligned16(d_o) || !aligned16(aux) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    CP_INVALID("cp_attn_bwd_prep: o, d_o and aux must be 16-byte aligned, lse 4-byte aligned");
+  int sms = 0;
+  cp_status st = require_sm103(nullptr, &sms);
+  if (st != CP_OK) return st;
+  return launch_bwd_prep(o, o_dtype == CP_BF16, d_o, do_dtype == CP_BF16, lse, sq, hq, d, aux, sms, stream);
+}
+
+CP_API cp_status cp_partial_attn_bwd(const cp_attn_bwd_desc* desc, cudaStream_t stream) {
+  clear_error();
+  if (desc == nullptr) CP_INVALID("cp_partial_attn_bwd: desc is NULL");
+  const cp_attn_bwd_desc& d = *desc;
+  if (d.in_dtype != CP_F32 && d.in_dtype != CP_BF16)
+    CP_INVALID("partial attention backward: in_dtype %d is not CP_F32 or CP_BF16", d.in_dtype);
+  if (d.sq < 0 || d.skv < 0) CP_INVALID("partial attention backward: negative token count");
+  if (d.sq > (int64_t(1) << 31) - 256 || d.skv > (int64_t(1) << 31) - 256)
+    CP_INVALID("partial attention backward: token counts must stay below 2^31");
+  if (d.hq <= 0 || d.hkv <= 0) CP_INVALID("partial attention backward: head counts must be positive");
+  if (d.hq % d.hkv != 0) CP_INVALID("partial attention backward: hq %d is not a multiple of hkv %d", d.hq, d.hkv);
+  if (d.d != 64 && d.d != 128) CP_INVALID("partial attention backward: head_dim %d not in {64, 128}", d.d);
+  if (d.causal != 0 && d.causal != 1) CP_INVALID("partial attention backward: causal must be 0 or 1");
+  if (d.q_pos.stride < 1 || d.kv_pos.stride < 1) CP_INVALID("partial attention backward: position strides must be >= 1");
+  if (d.q_pos.base < 0 || d.kv_pos.base < 0) CP_INVALID("partial attention backward: positions must be >= 0");
+  if (double(d.q_pos.base) + double(d.q_pos.stride) * double(d.sq) > 2.0e9 ||
+      double(d.kv_pos.base) + double(d.kv_pos.stride) * double(d.skv) > 2.0e9)
+    CP_INVALID("partial attention backward: global positions exceed 2e9");
+  if (!(d.scale >= 0.0f) || isinf(d.scale)) CP_INVALID("partial attention backward: scale must be finite and >= 0");
+  if (d.flags != 0) CP_INVALID("partial attention backward: unknown flag bits 0x%x", d.flags);
+  if (d.wait_timeout_ms < 0) CP_INVALID("partial attention backward: wait_timeout_ms must be >= 0");
+  if (d.sq == 0 || d.skv == 0) return CP_OK;  // nothing to add
+  if (d.q == nullptr || d.k == nullptr || d.v == nullptr || d.d_o == nullptr || d.aux == nullptr ||
+      d.dq == nullptr || d.dk == nullptr || d.dv == nullptr)
+    CP_INVALID("partial attention backward: q, k, v, d_o, aux, dq, dk and dv must not be NULL");
+  if (!aligned16(d.q) || !aligned16(d.k) || !aligned16(d.v) || !aligned16(d.d_o) || !aligned16(d.aux) ||
+      !aligned16(d.dq) || !aligned16(d.dk) || !aligned16(d.dv))
+    CP_INVALID("partial attention backward: every buffer must be 16-byte aligned");
+  int dev = 0, sms = 0;
+  cp_status st = require_sm103(&dev, &sms);
+  if (st != CP_OK) return st;
+  const float scale = d.scale > 0.0f ? d.scale : 1.0f / sqrtf(static_cast<float>(d.d));
+  const int64_t timeout_ns =
+      static_cast<int64_t>(d.wait_timeout_ms > 0 ? d.wait_timeout_ms : 2000) * 1000000LL;
+  if (d.in_dtype == CP_F32) return launch_partial_attn_bwd_simt(d, scale, stream);
+  return launch_partial_attn_bwd_tc(d, scale, timeout_ns, sms, stream);
+}
+
 CP_API cp_status cp_merge_partials(int32_t n, const float* const* o_parts,
                                    const float* const* lse_parts, int64_t sq, int32_t h, int32_t d,
                                    void* o_out, int32_t out_dtype, float* lse_out,

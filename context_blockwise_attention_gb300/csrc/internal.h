@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units (not part of the C ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -20,6 +21,12 @@ cp_status require_sm103(int* device_out, int* num_sms_out);
 // Maps a CUDA error to CP_ERR_CUDA with a message naming `what`.
 cp_status cuda_fail(cudaError_t e, const char* what);
 
+// 2-D tensor map over a token-major tensor viewed as [tokens, row_elems] (bf16 or fp32): box =
+// 128 bytes of columns x box_rows rows, 128-byte swizzle, zero fill out of bounds.  False if the
+// driver entry point is unavailable or the encoding is rejected.
+bool encode_map_2d(CUtensorMap* m, const void* base, int64_t tokens, int64_t row_elems, bool fp32,
+                   int box_rows);
+
 // ---- launchers (arguments already validated by the C entry points) ----
 cp_status launch_fill_positions(int32_t* out, int64_t n, int64_t base, int64_t stride,
                                 cudaStream_t s);
@@ -32,6 +39,13 @@ cp_status launch_partial_attn_tc(const cp_attn_desc& d, const cp_kv_chunk* chunk
                                  int64_t timeout_ns, int num_sms, cudaStream_t s);
 // O = 0, LSE = -inf for every row of desc's query shard (no visible key at all).
 cp_status launch_fill_empty(const cp_attn_desc& d, cudaStream_t s);
+
+// Backward pass (arguments validated by the entry points).
+cp_status launch_bwd_prep(const void* o, bool o_bf16, const void* d_o, bool do_bf16, const float* lse,
+                          int64_t sq, int32_t hq, int32_t d, float* aux, int num_sms, cudaStream_t s);
+cp_status launch_partial_attn_bwd_simt(const cp_attn_bwd_desc& d, float scale, cudaStream_t s);
+cp_status launch_partial_attn_bwd_tc(const cp_attn_bwd_desc& d, float scale, int64_t timeout_ns, int num_sms,
+                                     cudaStream_t s);
 
 struct MergeArgs {
   int32_t n;

@@ -32,7 +32,7 @@
 extern "C" {
 #endif
 
-#define CP_ABI_VERSION 2
+#define CP_ABI_VERSION 3
 /* Largest number of partials one cp_merge_partials call accepts. */
 #define CP_MAX_PARTIALS 128
 
@@ -235,6 +235,85 @@ cp_status cp_merge_partials(int32_t n, const float* const* o_parts, const float*
 cp_status cp_ulysses_reshard(int32_t dir, int32_t cp, int64_t seq_len, int32_t n_tensors,
                              const int32_t* heads, int32_t d, int32_t dtype, int32_t layout,
                              const void* const* in, void* const* out, cudaStream_t stream);
+
+/*
+ * ---------------------------------------------------------------- backward pass
+ * [PCP/DCP] section 2.3 (gradient handling): in training the gradients of the split sequence
+ * are split the same way and reduce-scattered across ranks; [Halo] (Ulysses): the backward pass
+ * runs the same exchanges in reverse.  What is differentiated is the partial attention above.
+ * For one (query shard, KV chunk) pair and one head, with the rows' FINAL (merged over every
+ * chunk) output O and LSE:
+ *     P_ij   = exp(scale * q_i . k_j - LSE_i)   visible pairs only; 0 when LSE_i = -inf
+ *     D_i    = dO_i . O_i                        (cp_attn_bwd_prep)
+ *     dV_j  += sum_i P_ij dO_i
+ *     dS_ij  = P_ij (dO_i . v_j - D_i)
+ *     dQ_i  += scale * sum_j dS_ij k_j
+ *     dK_j  += scale * sum_i dS_ij q_i
+ * A KV head's dK, dV sum over the Q heads of its group.  Summing dQ over a shard's chunks, and
+ * a chunk's dK, dV over every query shard that saw it (the pages' reduce-scatter, here a plain
+ * accumulation into the chunk owner's buffers), gives the gradients of unsharded attention.
+ */
+
+/* Floats of the per-row workspace cp_attn_bwd_prep writes for a query shard of sq rows, hq heads:
+ * [2][hq][sq rounded up to 128]. */
+#define CP_BWD_AUX_FLOATS(sq, hq) (2 * (int64_t)(hq) * ((((int64_t)(sq)) + 127) / 128 * 128))
+
+/*
+ * cp_attn_bwd_prep -- per query row and head, once per shard before its backward calls:
+ *   aux[0][h][i] = -LSE_ih * log2(e)  (-inf where LSE_ih = -inf: the row has no P)
+ *   aux[1][h][i] = -D_ih = -(dO_ih . O_ih)
+ * and -inf / 0 in the padding rows [sq, round_up(sq, 128)).
+ * Arguments:
+ *   o        device [sq, hq, d] final output of the shard (o_dtype CP_F32 or CP_BF16)
+ *   d_o      device [sq, hq, d] gradient of the loss w.r.t. that output (do_dtype CP_F32/CP_BF16)
+ *   lse      device fp32 [sq, hq] final LSE (natural log)
+ *   sq >= 0, hq >= 1, d in {64, 128}
+ *   aux      device fp32 [CP_BWD_AUX_FLOATS(sq, hq)], 16-byte aligned (caller-owned)
+ * Errors: CP_ERR_INVALID_ARG (null or misaligned pointers, bad sizes or dtypes),
+ *         CP_ERR_UNSUPPORTED, CP_ERR_CUDA.
+ */
+cp_status cp_attn_bwd_prep(const void* o, int32_t o_dtype, const void* d_o, int32_t do_dtype,
+                           const float* lse, int64_t sq, int32_t hq, int32_t d, float* aux,
+                           cudaStream_t stream);
+
+/*
+ * Backward of one (query shard, KV chunk) partial: ACCUMULATES (+=) the pair's share into
+ * dq [sq, hq, d], dk and dv [skv, hkv, d] (fp32, caller-owned, zeroed by the caller before the
+ * first call).  Fields as cp_attn_desc where the names match; also:
+ *   d_o       device [sq, hq, d], in_dtype (bf16: tensor-core path; fp32: CUDA-core path)
+ *   aux       the shard's cp_attn_bwd_prep output
+ *   dq, dk, dv  device fp32, 16-byte aligned
+ *   status, wait_timeout_ms  as cp_attn_desc (bounded in-kernel waits of the tensor-core path)
+ * Within one call dq, dk, dv are updated with atomic reductions (bf16 path) or by exclusive
+ * owners (fp32 path); calls on one stream follow stream order.  The summation order of dq and
+ * of a GQA group's dk, dv is not fixed on the bf16 path.
+ * Errors: CP_ERR_INVALID_ARG, CP_ERR_UNSUPPORTED, CP_ERR_CUDA.
+ */
+typedef struct {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* d_o;
+  int32_t in_dtype;
+  int32_t flags;
+  const float* aux;
+  float* dq;
+  float* dk;
+  float* dv;
+  int64_t sq;
+  int64_t skv;
+  int32_t hq;
+  int32_t hkv;
+  int32_t d;
+  int32_t causal;
+  float scale;
+  int32_t wait_timeout_ms;
+  cp_posmap q_pos;
+  cp_posmap kv_pos;
+  int32_t* status;
+} cp_attn_bwd_desc;
+
+cp_status cp_partial_attn_bwd(const cp_attn_bwd_desc* desc, cudaStream_t stream);
 
 /* Message for the calling thread's last non-OK status ("" if none).  Valid until the next call. */
 const char* cp_last_error(void);

@@ -53,3 +53,22 @@ def compare_partial(o_gpu, l_gpu, o_ref, l_ref, tol_o, tol_l, what=""):
     assert eo <= tol_o, f"{what}: max|dO| = {eo:.3e} > {tol_o}"
     assert el <= tol_l, f"{what}: max|dLSE| = {el:.3e} > {tol_l}"
     return eo, el
+
+
+# Gradients (backward pass): max-abs error relative to the tensor's own scale, max(1, max|ref|).
+# fp32 inputs: fp32 accumulation only.  bf16 inputs: P and dS are rounded to bf16 (relative
+# 2^-9 each) before the dV, dK and dQ products.
+TOL_GRAD_F32 = 1e-5
+TOL_GRAD_BF16 = 1e-2
+
+
+def compare_grad(g_gpu, g_ref, tol, what=""):
+    g_gpu = np.asarray(g_gpu, dtype=np.float64)
+    g_ref = np.asarray(g_ref, dtype=np.float64)
+    assert g_gpu.shape == g_ref.shape, f"{what}: shape {g_gpu.shape} != {g_ref.shape}"
+    assert np.all(np.isfinite(g_gpu)), f"{what}: non-finite gradient"
+    scale = max(1.0, float(np.abs(g_ref).max()) if g_ref.size else 1.0)
+    err = float(np.abs(g_gpu - g_ref).max()) / scale if g_ref.size else 0.0
+    assert err <= tol, f"{what}: max|err|/scale = {err:.3e} > {tol} (scale {scale:.3g})"
+    return err
+

@@ -23,7 +23,7 @@ def test_exports_every_declared_function():
 
 
 def test_version():
-    assert cpa.version() == 2
+    assert cpa.version() == 3
 
 
 def test_desc_layout_matches_header():
@@ -207,3 +207,48 @@ def test_reshard_rejects_two_block_odd_length():
     # 36 % 4 == 0 but 36 % 8 != 0
     assert lib.cp_ulysses_reshard(0, 4, 36, 1, heads, 64, 1, api.CP_LAYOUT_TWO_BLOCK, ptrs, ptrs,
                                   None) == api.CP_ERR_INVALID_ARG
+
+
+def test_bwd_desc_layout_matches_header():
+    assert ctypes.sizeof(api._AttnBwdDesc) == 152
+    assert api._AttnBwdDesc.aux.offset == 40 and api._AttnBwdDesc.q_pos.offset == 112
+
+
+def _bwd_desc(**kw):
+    d = api._AttnBwdDesc()
+    d.q = d.k = d.v = d.d_o = 0x1000
+    d.aux = d.dq = d.dk = d.dv = 0x2000
+    d.in_dtype = api.CP_BF16
+    d.sq, d.skv, d.hq, d.hkv, d.d = 128, 128, 8, 2, 128
+    d.causal = 1
+    d.q_pos = api._PosMap(0, 1)
+    d.kv_pos = api._PosMap(0, 1)
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+@pytest.mark.parametrize("field,value", [
+    ("d", 96), ("hq", 5), ("hkv", 0), ("in_dtype", 4), ("causal", 3), ("q", 0), ("aux", 0),
+    ("dq", 0), ("dk", 0x2004), ("sq", -1), ("skv", -2), ("flags", 1),
+    ("q_pos", api._PosMap(0, 0)), ("kv_pos", api._PosMap(-1, 1)), ("scale", float("inf")),
+    ("wait_timeout_ms", -1),
+])
+def test_partial_attn_bwd_rejects(field, value):
+    lib = cpa.load_library()
+    d = _bwd_desc(**{field: value})
+    assert lib.cp_partial_attn_bwd(ctypes.byref(d), None) == api.CP_ERR_INVALID_ARG
+    assert lib.cp_last_error()
+    assert lib.cp_partial_attn_bwd(None, None) == api.CP_ERR_INVALID_ARG
+
+
+def test_bwd_prep_rejects():
+    lib = cpa.load_library()
+    p = ctypes.c_void_p(0x1000)
+    assert lib.cp_attn_bwd_prep(p, 7, p, 1, p, 16, 2, 64, p, None) == api.CP_ERR_INVALID_ARG   # o dtype
+    assert lib.cp_attn_bwd_prep(p, 0, p, 1, p, 16, 2, 96, p, None) == api.CP_ERR_INVALID_ARG   # d
+    assert lib.cp_attn_bwd_prep(p, 0, p, 1, p, 16, 0, 64, p, None) == api.CP_ERR_INVALID_ARG   # hq
+    assert lib.cp_attn_bwd_prep(p, 0, p, 1, None, 16, 2, 64, p, None) == api.CP_ERR_INVALID_ARG  # lse
+    assert lib.cp_attn_bwd_prep(p, 0, p, 1, p, 16, 2, 64, ctypes.c_void_p(0x1004), None) == \
+        api.CP_ERR_INVALID_ARG  # aux alignment
+    assert cpa.bwd_aux_floats(130, 3) == 2 * 3 * 256
