@@ -82,6 +82,9 @@ class Step:
         self.call_meta = []
         self.rank_plans = []      # (query rank, q shard, merged out, merged lse) per query rank
         self.fused_meta = []      # query rank of each fused call
+        # per query block, in order: (query rank, q block, out block, lse block, q map,
+        # [(source rank, first source row, keys, kv map) of the visible chunks, arrival order])
+        self.blocks = []
         self.merges = []          # list of (o_parts, l_parts, o_out, l_out)
         self.host_inputs = []     # (host pinned, device) pairs copied in e2e mode
         self.host_outputs = []    # (device, host pinned) pairs read back in e2e mode
@@ -140,7 +143,7 @@ class Step:
             row = 0
             for qmap, nq in qsegs:
                 qs = q[row:row + nq]
-                o_parts, l_parts, seg_calls = [], [], []
+                o_parts, l_parts, seg_calls, seg_chunks = [], [], [], []
                 for ci in order:
                     src, lo, nk, kmap = plan[int(ci)]
                     n_vis = cpa.visible_pairs(qmap, nq, kmap, nk, w.causal)
@@ -152,12 +155,14 @@ class Step:
                     seg_calls.append(dict(q=qs, k=k[lo:lo + nk], v=v[lo:lo + nk], q_pos=qmap,
                                           kv_pos=kmap, causal=w.causal, o=o, lse=l))
                     self.call_meta.append((qr, row, nq, src, lo, nk))
+                    seg_chunks.append((src, lo, nk, kmap))
                     self.flops += 4 * w.d * w.hq * n_vis
                     o_parts.append(o)
                     l_parts.append(l)
                     fr = cpa.finite_rows(qmap, nq, kmap, nk, w.causal)
                     self.merge_bytes += nq * w.hq * 4 + fr * w.hq * w.d * 4
                 o_seg, l_seg = out[row:row + nq], lse[row:row + nq]
+                self.blocks.append((qr, qs, o_seg, l_seg, qmap, seg_chunks))
                 if self.fused:
                     # the block's chunks, in arrival order, in one launch; no partials, no merge
                     self.fused_calls.append(dict(q=qs, chunks=[(c["k"], c["v"], c["kv_pos"]) for c in seg_calls],
@@ -283,6 +288,60 @@ class Step:
     @property
     def d2h_bytes(self):
         return sum(h.numel() * h.element_size() for _, h in self.host_outputs)
+
+
+class BwdStep:
+    """Backward of a step's attention: per query block the prep kernel (from the
+    block's final O and LSE, produced by running `fwd` once), then one partial backward per
+    (query block, visible chunk) pair in arrival order; dQ accumulates per block, dK and dV into
+    the chunk owner's shard buffers (the pages' reduce-scatter).  Gradients are zeroed inside the
+    step, as a training step would."""
+
+    def __init__(self, fwd, seed=4242):
+        import context_blockwise_attention_gb300 as cpa
+        from context_blockwise_attention_gb300 import workloads as wl
+        self.cpa = cpa
+        w = fwd.w
+        dev = fwd.device
+        fwd.run()
+        torch.cuda.synchronize()
+        self.dk = {r: torch.zeros(k.shape, dtype=torch.float32, device=dev) for r, (k, _) in fwd.kv.items()}
+        self.dv = {r: torch.zeros(k.shape, dtype=torch.float32, device=dev) for r, (k, _) in fwd.kv.items()}
+        self.dqs = []
+        self.preps = []
+        self.calls = []
+        self.flops = 0
+        for i, (qr, qb, ob, lb, qmap, chunks) in enumerate(fwd.blocks):
+            nq = qb.shape[0]
+            d_o = wl.normal(tuple(qb.shape), qb.dtype, seed + 31 * i, 1.0, device=dev)
+            aux = torch.empty(cpa.bwd_aux_floats(nq, w.hq), dtype=torch.float32, device=dev)
+            dq = torch.zeros(tuple(qb.shape), dtype=torch.float32, device=dev)
+            self.dqs.append(dq)
+            self.preps.append(dict(o=ob, d_o=d_o, lse=lb, aux=aux))
+            for src, lo, nk, kmap in chunks:
+                k, v = fwd.kv[src]
+                self.calls.append(dict(q=qb, k=k[lo:lo + nk], v=v[lo:lo + nk], d_o=d_o, aux=aux, q_pos=qmap,
+                                       kv_pos=kmap, dq=dq, dk=self.dk[src][lo:lo + nk],
+                                       dv=self.dv[src][lo:lo + nk], causal=w.causal))
+                # five products of 2*D flops per visible pair: S, dP, dV, dK, dQ
+                self.flops += 10 * w.d * w.hq * cpa.visible_pairs(qmap, nq, kmap, nk, w.causal)
+
+    def run(self, timers=None):
+        stream = torch.cuda.current_stream()
+        for t in list(self.dk.values()) + list(self.dv.values()) + self.dqs:
+            t.zero_()
+        for kw in self.preps:
+            self.cpa.attn_bwd_prep(**kw)
+        if timers is not None:
+            a = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+        for kw in self.calls:
+            self.cpa.partial_attn_bwd(**kw)
+        if timers is not None:
+            b = torch.cuda.Event(enable_timing=True)
+            b.record(stream)
+            timers.append((a, b))
+        return len(self.preps) + len(self.calls)
 
 
 # ----------------------------------------------------------------------------- measurement
@@ -610,6 +669,35 @@ def run_gpu(args):
                  "launches_per_step": len(fstep.fused_calls),
                  "path": "one cp_partial_attn_chunks per query block (no partials, no merge)"}
         del fstep
+    backward = None
+    if args.config != 4 and w.dtype == "bf16" and not args.no_backward:
+        # the backward of the same workload (f4), timed the same way (L2 flushed per step)
+        bstep = BwdStep(Step(args.config, dev, query_rank=qr, layout=layout, fused=True))
+        for _ in range(args.warmup):
+            bstep.run()
+        barrier()
+        bms, btimes, blaunch = [], [], 0
+        for _ in range(args.steps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            blaunch += bstep.run(btimes)
+            b.record(stream)
+            torch.cuda.synchronize()
+            bms.append(a.elapsed_time(b))
+        barrier()
+        b_ms, b_value = aggregate(sum(bms), bstep.flops, args.steps, world, dev)
+        b_kernel_ms = sum(s_.elapsed_time(e_) for s_, e_ in btimes) / args.steps
+        b_ach = bstep.flops / (b_kernel_ms * 1e-3) / 1e12
+        backward = {"value": b_value, "unit": "TFLOP/s", "ms_per_step": b_ms,
+                    "step_flop": bstep.flops, "flop_per_visible_pair": 10 * w.d * w.hq,
+                    "kernel": "attn_bwd_tc_kernel", "kernel_ms_per_step": b_kernel_ms,
+                    "achieved": b_ach, "peak": peaks["bf16"], "frac": b_ach / peaks["bf16"],
+                    "launches_per_step": blaunch // args.steps,
+                    "path": "prep per query block + one cp_partial_attn_bwd per (block, chunk); "
+                            "dK/dV accumulated into the chunk owners' shards; gradients zeroed in the step"}
+        del bstep
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         t, fl, desc = oracle_sample(args.config, args.ref_rows, layout=layout)
@@ -629,7 +717,8 @@ def run_gpu(args):
                         "d2h_bytes_per_step": step.d2h_bytes,
                         "ms_per_step": e2e_ms_per_step},
                 "gpu_launches": launches,
-                "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks, "fused": fused, **extra}
+                "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks, "fused": fused,
+                "backward": backward, **extra}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -792,6 +881,8 @@ def main():
                     help="skip the extra measurement of the fused chunk-list path")
     ap.add_argument("--fused", action="store_true",
                     help="consume each rank's chunks in one launch (no partials, no merge)")
+    ap.add_argument("--no-backward", action="store_true",
+                    help="skip the extra measurement of the backward pass")
     ap.add_argument("--pipelined", action="store_true",
                     help="chunk arrival (host copies on a second stream) overlapped with compute")
     ap.add_argument("--seq-len", type=int, default=None,

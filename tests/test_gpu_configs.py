@@ -13,7 +13,7 @@ import torch
 
 import helpers
 import oracle
-from helpers import TOL_BF16_LSE, TOL_BF16_O, TOL_F32, compare_partial
+from helpers import TOL_BF16_LSE, TOL_BF16_O, TOL_F32, TOL_GRAD_BF16, compare_grad, compare_partial
 
 pytestmark = pytest.mark.gpu
 
@@ -199,3 +199,42 @@ def test_cfg4_ulysses():
         final = np.stack([step.xo[t // local][t % local, r * hl:(r + 1) * hl].float().cpu().numpy()
                           for t in rows])
         assert helpers.max_abs(final, o_ref) <= TOL_BF16_O, f"cfg4 final output, heads of rank {r}"
+
+
+def test_cfg2_backward_sampled():
+    # the backward of workload 2 (rank 7, 8 chunks) as the bench times it: GPU forward (fused),
+    # prep, one partial backward per chunk.  The oracle computes the rows' final O and LSE itself
+    # (all rows, all keys), then the exact gradients on samples: dQ on sampled rows (against
+    # every chunk), dK and dV on sampled keys of every shard (against every row)
+    w = wl.WORKLOADS[2]
+    fstep = bench.Step(2, DEV, fused=True)
+    bstep = bench.BwdStep(fstep)
+    bstep.run()
+    torch.cuda.synchronize()
+    assert len(fstep.blocks) == 1
+    qr, qb, _, _, _, _ = fstep.blocks[0]
+    layout = w.layout
+    qpos = oracle.shard_positions(w.seq_len, w.cp, qr, layout)
+    q_cpu = qb.cpu()
+    d_o = bstep.preps[0]["d_o"].cpu()
+    kv_cpu = {r: (k.cpu(), v.cpu()) for r, (k, v) in fstep.kv.items()}
+    spos = {r: oracle.shard_positions(w.seq_len, w.cp, r, layout) for r in range(w.cp)}
+    k_all = torch.cat([kv_cpu[r][0] for r in range(w.cp)])
+    v_all = torch.cat([kv_cpu[r][1] for r in range(w.cp)])
+    o_ref, l_ref = oracle.attention(q_cpu, k_all, v_all, qpos, np.concatenate([spos[r] for r in range(w.cp)]),
+                                    causal=True)
+    rows = _rows_for(w, w.local_len + qr, 256)
+    ri = torch.from_numpy(rows)
+    dq_ref = np.zeros((len(rows), w.hq, w.d))
+    for r in range(w.cp):
+        dq_ref += oracle.chunk_backward(q_cpu[ri], kv_cpu[r][0], kv_cpu[r][1], d_o[ri], o_ref[rows],
+                                        l_ref[rows], qpos[rows], spos[r], causal=True)[0]
+    compare_grad(bstep.dqs[0].cpu().numpy()[rows], dq_ref, TOL_GRAD_BF16, "cfg2 dQ (sampled rows)")
+    keys = wl.sample_rows(w.local_len, 64, seed=3, must=[0, 127, 128, w.local_len - 1])
+    ki = torch.from_numpy(keys)
+    for r in range(w.cp):
+        _, dk_ref, dv_ref = oracle.chunk_backward(q_cpu, kv_cpu[r][0][ki], kv_cpu[r][1][ki], d_o, o_ref, l_ref,
+                                                  qpos, spos[r][keys], causal=True)
+        compare_grad(bstep.dk[r].cpu().numpy()[keys], dk_ref, TOL_GRAD_BF16, f"cfg2 dK shard {r} (sampled keys)")
+        compare_grad(bstep.dv[r].cpu().numpy()[keys], dv_ref, TOL_GRAD_BF16, f"cfg2 dV shard {r} (sampled keys)")
+
