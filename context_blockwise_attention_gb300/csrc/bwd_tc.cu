@@ -58,6 +58,8 @@ enum BwdSite : int {
   kSDqFree = 10,
   kSAccFull = 11,
   kSAccEmpty = 12,
+  kSDoFull = 13,
+  kSDoEmpty = 14,
 };
 
 struct BwdParams {
@@ -77,24 +79,27 @@ struct BLayout {
   static constexpr int kChunkBytes = 128 * 128;     // 128 rows x 128 bytes
   static constexpr int kTileBytes = kRows * D * 2;  // bf16 [128, D]
   static constexpr int kChunks = D / 64;
-  static constexpr int kQStages = (D == 64) ? 2 : 1;
+  static constexpr int kQStages = 2;                // Q tile + the rows' aux runs
+  static constexpr int kDoStages = (D == 64) ? 2 : 1;
+  static constexpr int kStageBufs = (D == 64) ? 2 : 1;  // reduction staging boxes per warp
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTileBytes;
   static constexpr int kOffQ = 2 * kTileBytes;
   static constexpr int kOffDO = kOffQ + kQStages * kTileBytes;
-  static constexpr int kOffDS = kOffDO + kQStages * kTileBytes;  // dS, 128 keys x 128 queries bf16
-  static constexpr int kOffAux = kOffDS + 2 * kChunkBytes;       // per stage: 128 + 128 floats
-  static constexpr int kOffStage = kOffAux + kQStages * 1024;    // 4 warps x 2 x 4 KB
-  static constexpr int kOffBar = kOffStage + 8 * 4096;
-  // kv_full, kv_empty, q_full[S], q_empty[S], s_full, p_ready, dp_full, ds_ready, dq_full,
-  // dq_free, acc_full, acc_empty, drain
-  static constexpr int kNumBars = 2 + 2 * kQStages + 9;
+  static constexpr int kOffDS = kOffDO + kDoStages * kTileBytes;  // dS, 128 keys x 128 queries bf16
+  static constexpr int kOffAux = kOffDS + 2 * kChunkBytes;        // per Q stage: 128 + 128 floats
+  static constexpr int kOffStage = kOffAux + kQStages * 1024;     // 4 warps x kStageBufs x 4 KB
+  static constexpr int kOffBar = kOffStage + 4 * kStageBufs * 4096;
+  // kv_full, kv_empty, q_full[Q], q_empty[Q], do_full[DO], do_empty[DO], s_full, p_ready, dp_full,
+  // ds_ready, dq_full, dq_free, acc_full, acc_empty, drain
+  static constexpr int kNumBars = 2 + 2 * kQStages + 2 * kDoStages + 9;
   static constexpr int kOffCtl = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffCtl + 16;
   static constexpr int kSmemLaunch = kBytes + 1024;
-  // tensor memory columns
+  // tensor memory columns; dQ: own columns at D=64, the dP^T columns at D=128 (free once the
+  // dK product has consumed dS^T, and read out before the next dP^T)
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
-  static constexpr uint32_t kColDQ = (D == 64) ? 384 : 0;
+  static constexpr uint32_t kColDQ = (D == 64) ? 384 : 128;
 };
 static_assert(BLayout<128>::kSmemLaunch <= 232448, "shared memory budget (D=128)");
 static_assert(BLayout<64>::kSmemLaunch <= 232448, "shared memory budget (D=64)");
@@ -108,7 +113,7 @@ constexpr uint32_t kRegsRed = 136;
 static_assert(4 * kRegsControl + 4 * kRegsGrad + 4 * kRegsRed == 12 * 168, "register split must match launch");
 
 struct Bars {
-  uint32_t kv_full, kv_empty, q_full, q_empty;  // q_*: stage 0, +8 per stage
+  uint32_t kv_full, kv_empty, q_full, q_empty, do_full, do_empty;  // q_*, do_*: stage 0, +8 per stage
   uint32_t s_full, p_ready, dp_full, ds_ready, dq_full, dq_free, acc_full, acc_empty, drain;
 };
 
@@ -135,13 +140,20 @@ __device__ __forceinline__ BUnit decode_bunit(const BwdParams& p, int64_t u) {
 }
 
 // One warp's bulk reduction: 32 fp32 columns of its 32 rows, times `mul`, staged in one of its
-// two 4 KB swizzled boxes and added into `tm` at (x, y).  Rows past `rows` are clipped by the
+// BUFS 4 KB swizzled boxes and added into `tm` at (x, y).  Rows past `rows` are clipped by the
 // tensor map; a box that starts past them is skipped.  Returns the updated reduction count.
+template <int BUFS>
 __device__ __forceinline__ uint32_t reduce_box(uint32_t stage0, int lane, uint32_t nred, const uint32_t (&v)[32],
                                                float mul, const CUtensorMap* tm, int32_t x, int32_t y, int64_t rows) {
   if (y >= rows) return nred;
-  const uint32_t sb = stage0 + (nred & 1u) * 4096u;
-  if (lane == 0) ptx::bulk_wait_read_1();  // the reduction that used this buffer has read it
+  const uint32_t sb = stage0 + (nred % BUFS) * 4096u;
+  // the reduction that used this buffer last has finished reading it
+  if (lane == 0) {
+    if (BUFS == 2)
+      ptx::bulk_wait_read_1();
+    else
+      ptx::bulk_wait_read_all();
+  }
   __syncwarp();
   const uint32_t row = sb + static_cast<uint32_t>(lane) * 128u;
   const uint32_t sw = static_cast<uint32_t>(lane & 7);
@@ -181,7 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   b.kv_empty = b.kv_full + 8;
   b.q_full = b.kv_empty + 8;
   b.q_empty = b.q_full + 8 * L::kQStages;
-  b.s_full = b.q_empty + 8 * L::kQStages;
+  b.do_full = b.q_empty + 8 * L::kQStages;
+  b.do_empty = b.do_full + 8 * L::kDoStages;
+  b.s_full = b.do_empty + 8 * L::kDoStages;
   b.p_ready = b.s_full + 8;
   b.dp_full = b.p_ready + 8;
   b.ds_ready = b.dp_full + 8;
@@ -201,6 +215,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < L::kQStages; ++s) {
       ptx::mbar_init(b.q_full + 8 * s, 1);
       ptx::mbar_init(b.q_empty + 8 * s, 1);
+    }
+    for (int s = 0; s < L::kDoStages; ++s) {
+      ptx::mbar_init(b.do_full + 8 * s, 1);
+      ptx::mbar_init(b.do_empty + 8 * s, 1);
     }
     ptx::mbar_init(b.s_full, 1);
     ptx::mbar_init(b.p_ready, 4);
@@ -241,6 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tma_prefetch_desc(&tm_v);
       }
       int64_t gi = 0, ku = 0;  // query tiles and units with work issued so far
+      int64_t ql = 0, dl = 0;  // Q and dO loads issued
       bool ok = true;
       for (int64_t k = 0; ok; ++k) {
         const int64_t u = unit_of(k, cta, grid);
@@ -263,29 +282,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = wait_warp(b.q_empty + 8 * st, ph ^ 1, ctl, kSQEmpty))) break;
           if (leader) {
             const uint32_t full = b.q_full + 8 * st;
-            ptx::mbar_arrive_expect_tx(full, 2 * L::kTileBytes + 1024);
-            for (int cc = 0; cc < L::kChunks; ++cc) {
+            ptx::mbar_arrive_expect_tx(full, L::kTileBytes + 1024);
+            for (int cc = 0; cc < L::kChunks; ++cc)
               ptx::tma_load_2d(sQ + st * L::kTileBytes + cc * L::kChunkBytes, &tm_q, w.h * D + cc * 64,
                                t * kRows, full);
-              ptx::tma_load_2d(sDO + st * L::kTileBytes + cc * L::kChunkBytes, &tm_do, w.h * D + cc * 64,
-                               t * kRows, full);
-            }
             const float* a0 = p.aux + static_cast<int64_t>(w.h) * p.sq_pad + static_cast<int64_t>(t) * kRows;
             const float* a1 = p.aux + (static_cast<int64_t>(p.hq) + w.h) * p.sq_pad + static_cast<int64_t>(t) * kRows;
             ptx::bulk_load(sAux + st * 1024, a0, 512, full);
             ptx::bulk_load(sAux + st * 1024 + 512, a1, 512, full);
           }
           __syncwarp();
+          ql = gi + 1;
+          const int sd = static_cast<int>(gi % L::kDoStages);
+          const uint32_t phd = static_cast<uint32_t>((gi / L::kDoStages) & 1);
+          if (!(ok = wait_warp(b.do_empty + 8 * sd, phd ^ 1, ctl, kSDoEmpty))) break;
+          if (leader) {
+            const uint32_t full = b.do_full + 8 * sd;
+            ptx::mbar_arrive_expect_tx(full, L::kTileBytes);
+            for (int cc = 0; cc < L::kChunks; ++cc)
+              ptx::tma_load_2d(sDO + sd * L::kTileBytes + cc * L::kChunkBytes, &tm_do, w.h * D + cc * 64,
+                               t * kRows, full);
+          }
+          __syncwarp();
+          dl = gi + 1;
         }
         ++ku;
       }
       if (*abort_flag && leader) {
         // loads in flight must land before the CTA's shared memory goes away
         if (ku > 0) wait_drain(b.kv_full, static_cast<uint32_t>((ku - 1) & 1), p.timeout_ns);
+        // the last load issued into every stage: load n went to stage n % S, phase (n / S) & 1
         for (int s = 0; s < L::kQStages; ++s) {
-          const int64_t last = (gi - 1 - s >= 0) ? gi - 1 - ((gi - 1 - s) % L::kQStages) : -1;
+          const int64_t last = (ql - 1 - s >= 0) ? ql - 1 - ((ql - 1 - s) % L::kQStages) : -1;
           if (last >= 0)
             wait_drain(b.q_full + 8 * s, static_cast<uint32_t>((last / L::kQStages) & 1), p.timeout_ns);
+        }
+        for (int s = 0; s < L::kDoStages; ++s) {
+          const int64_t last = (dl - 1 - s >= 0) ? dl - 1 - ((dl - 1 - s) % L::kDoStages) : -1;
+          if (last >= 0)
+            wait_drain(b.do_full + 8 * s, static_cast<uint32_t>((last / L::kDoStages) & 1), p.timeout_ns);
         }
       }
       __syncwarp();
@@ -328,6 +363,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                       kIdescQ, kk > 0 ? 1u : 0u);
       };
 
+      // Per query tile gi of a unit: [S^T(gi) if first of the unit] dP^T(gi), dV(gi), S^T(gi+1) of
+      // the same unit (overlaps the gradient warps' dS(gi)), dK(gi), dQ(gi).
+      auto issue_s = [&](int64_t g) -> bool {
+        const int sq = static_cast<int>(g % L::kQStages);
+        if (!wait_warp(b.q_full + 8 * sq, static_cast<uint32_t>((g / L::kQStages) & 1), ctl, kSQFull)) return false;
+        ptx::tc_fence_after();
+        if (leader) {
+          issue_kk(tmem + L::kColS, dK_k, dQ_k + sq * kTileUnits);
+          ptx::mma_commit(b.s_full);
+        }
+        __syncwarp();
+        return true;
+      };
       int64_t gi = 0, ku = 0;
       bool ok = true;
       for (int64_t k = 0; ok; ++k) {
@@ -336,20 +384,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const BUnit w = decode_bunit(p, u);
         if (w.nit <= 0) continue;
         if (!(ok = wait_warp(b.kv_full, static_cast<uint32_t>(ku & 1), ctl, kSKvFull))) break;
+        if (!(ok = issue_s(gi))) break;
         for (int it = 0; it < w.nit; ++it, ++gi) {
           const bool first = (it == 0);
           const int st = static_cast<int>(gi % L::kQStages);
-          const uint32_t ph = static_cast<uint32_t>((gi / L::kQStages) & 1);
+          const int sd = static_cast<int>(gi % L::kDoStages);
+          const uint32_t phd = static_cast<uint32_t>((gi / L::kDoStages) & 1);
           const uint32_t prev = static_cast<uint32_t>((gi - 1) & 1);
           const uint32_t cur = static_cast<uint32_t>(gi & 1);
-          if (!(ok = wait_warp(b.q_full + 8 * st, ph, ctl, kSQFull))) break;
-          // D = 128: the previous dQ sits in the S^T columns until the reduction warps read it
+          if (!(ok = wait_warp(b.do_full + 8 * sd, phd, ctl, kSDoFull))) break;
+          // D = 128: the previous dQ sits in the dP^T columns until the reduction warps read it
           if (D == 128 && gi > 0 && !(ok = wait_warp(b.dq_free, prev, ctl, kSDqFree))) break;
           ptx::tc_fence_after();
           if (leader) {
-            issue_kk(tmem + L::kColS, dK_k, dQ_k + st * kTileUnits);
-            ptx::mma_commit(b.s_full);
-            issue_kk(tmem + L::kColDP, dV_k, dDO_k + st * kTileUnits);
+            issue_kk(tmem + L::kColDP, dV_k, dDO_k + sd * kTileUnits);
             ptx::mma_commit(b.dp_full);
           }
           __syncwarp();
@@ -358,8 +406,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (first && ku > 0 && !(ok = wait_warp(b.acc_empty, static_cast<uint32_t>((ku - 1) & 1), ctl, kSAccEmpty)))
             break;
           ptx::tc_fence_after();
-          if (leader) issue_ts(tmem + L::kColDV, tmem + L::kColS, dDO_mn + st * kTileUnits, !first);
+          if (leader) {
+            issue_ts(tmem + L::kColDV, tmem + L::kColS, dDO_mn + sd * kTileUnits, !first);
+            ptx::mma_commit(b.do_empty + 8 * sd);
+          }
           __syncwarp();
+          // the next S^T may overwrite P^T: the dV product just issued reads it first (issue order)
+          if (it + 1 < w.nit && !(ok = issue_s(gi + 1))) break;
           if (!(ok = wait_warp(b.ds_ready, cur, ctl, kSDsReady))) break;
           ptx::tc_fence_after();
           if (leader) issue_ts(tmem + L::kColDK, tmem + L::kColDP, dQ_mn + st * kTileUnits, !first);
@@ -427,38 +480,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = wait_warp(b.q_full + 8 * st, static_cast<uint32_t>((gi / L::kQStages) & 1), ctl, kSQFull))) break;
         if (!(ok = wait_warp(b.s_full, cur, ctl, kSSFull))) break;
         ptx::tc_fence_after();
-        float pf[kRows];
+        // all 128 columns of S^T in one go (one wait), then P in place
+        uint32_t pf[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + c * 32, pf[c]);
+        ptx::tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t sr[32];
-          ptx::tmem_ld32(tS + c * 32, sr);
-          ptx::tmem_wait_ld();
-          uint32_t pk[16];
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
             const float4 nl = ptx::lds128(a_nl + (c * 32 + e4 * 4) * 4);
             const uint64_t x01 = ptx::f2_fma(
-                ptx::f2_pack(__uint_as_float(sr[4 * e4]), __uint_as_float(sr[4 * e4 + 1])), sl2x2,
+                ptx::f2_pack(__uint_as_float(pf[c][4 * e4]), __uint_as_float(pf[c][4 * e4 + 1])), sl2x2,
                 ptx::f2_pack(nl.x, nl.y));
             const uint64_t x23 = ptx::f2_fma(
-                ptx::f2_pack(__uint_as_float(sr[4 * e4 + 2]), __uint_as_float(sr[4 * e4 + 3])), sl2x2,
+                ptx::f2_pack(__uint_as_float(pf[c][4 * e4 + 2]), __uint_as_float(pf[c][4 * e4 + 3])), sl2x2,
                 ptx::f2_pack(nl.z, nl.w));
             float x0, x1, x2, x3;
             ptx::f2_unpack(x01, x0, x1);
             ptx::f2_unpack(x23, x2, x3);
-            const int col = c * 32 + e4 * 4;
-            pf[col] = ptx::ex2(x0);
-            pf[col + 1] = ptx::ex2(x1);
-            pf[col + 2] = ptx::ex2(x2);
-            pf[col + 3] = ptx::ex2(x3);
+            pf[c][4 * e4] = __float_as_uint(ptx::ex2(x0));
+            pf[c][4 * e4 + 1] = __float_as_uint(ptx::ex2(x1));
+            pf[c][4 * e4 + 2] = __float_as_uint(ptx::ex2(x2));
+            pf[c][4 * e4 + 3] = __float_as_uint(ptx::ex2(x3));
           }
           if (cmin > c * 32) {
 #pragma unroll
             for (int e = 0; e < 32; ++e)
-              if (c * 32 + e < cmin) pf[c * 32 + e] = 0.0f;
+              if (c * 32 + e < cmin) pf[c][e] = 0u;
           }
+          uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) pk[e] = ptx::pack_bf16x2(pf[c * 32 + 2 * e], pf[c * 32 + 2 * e + 1]);
+          for (int e = 0; e < 16; ++e)
+            pk[e] = ptx::pack_bf16x2(__uint_as_float(pf[c][2 * e]), __uint_as_float(pf[c][2 * e + 1]));
           ptx::tmem_st16(tS + c * 16, pk);
         }
         ptx::tmem_wait_st();
@@ -484,8 +538,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ptx::f2_pack(nd.x, nd.y));
             const uint64_t t23 = ptx::f2_add(
                 ptx::f2_pack(__uint_as_float(dr[4 * e4 + 2]), __uint_as_float(dr[4 * e4 + 3])), ptx::f2_pack(nd.z, nd.w));
-            const uint64_t d01 = ptx::f2_mul(ptx::f2_pack(pf[col], pf[col + 1]), t01);
-            const uint64_t d23 = ptx::f2_mul(ptx::f2_pack(pf[col + 2], pf[col + 3]), t23);
+            const uint64_t d01 = ptx::f2_mul(
+                ptx::f2_pack(__uint_as_float(pf[c][4 * e4]), __uint_as_float(pf[c][4 * e4 + 1])), t01);
+            const uint64_t d23 = ptx::f2_mul(
+                ptx::f2_pack(__uint_as_float(pf[c][4 * e4 + 2]), __uint_as_float(pf[c][4 * e4 + 3])), t23);
             float s0, s1, s2, s3;
             ptx::f2_unpack(d01, s0, s1);
             ptx::f2_unpack(d23, s2, s3);
@@ -513,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ reduction warpgroup
     const int wq = warp & 3;
     const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t stage0 = sbase + L::kOffStage + static_cast<uint32_t>(wq) * 2u * 4096u;
+    const uint32_t stage0 = sbase + L::kOffStage + static_cast<uint32_t>(wq * L::kStageBufs) * 4096u;
     int64_t gi = 0, ku = 0;
     uint32_t nred = 0;  // bulk reductions issued by this warp (staging double buffer)
     bool ok = true;
@@ -539,8 +595,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(b.dq_free);
           }
-          nred = reduce_box(stage0, lane, nred, v0, p.scale, &tm_dq, w.h * D + c2 * 64, t * kRows + wq * 32, p.sq);
-          nred = reduce_box(stage0, lane, nred, v1, p.scale, &tm_dq, w.h * D + c2 * 64 + 32, t * kRows + wq * 32,
+          nred = reduce_box<L::kStageBufs>(stage0, lane, nred, v0, p.scale, &tm_dq, w.h * D + c2 * 64, t * kRows + wq * 32, p.sq);
+          nred = reduce_box<L::kStageBufs>(stage0, lane, nred, v1, p.scale, &tm_dq, w.h * D + c2 * 64 + 32, t * kRows + wq * 32,
                             p.sq);
         }
       }
@@ -553,14 +609,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t v[32];
         ptx::tmem_ld32(tmem + L::kColDK + lane_bits + c * 32, v);
         ptx::tmem_wait_ld();
-        nred = reduce_box(stage0, lane, nred, v, p.scale, &tm_dk, w.g * D + c * 32, w.jt * kKeys + wq * 32, p.skv);
+        nred = reduce_box<L::kStageBufs>(stage0, lane, nred, v, p.scale, &tm_dk, w.g * D + c * 32, w.jt * kKeys + wq * 32, p.skv);
       }
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
         ptx::tmem_ld32(tmem + L::kColDV + lane_bits + c * 32, v);
         ptx::tmem_wait_ld();
-        nred = reduce_box(stage0, lane, nred, v, 1.0f, &tm_dv, w.g * D + c * 32, w.jt * kKeys + wq * 32, p.skv);
+        nred = reduce_box<L::kStageBufs>(stage0, lane, nred, v, 1.0f, &tm_dv, w.g * D + c * 32, w.jt * kKeys + wq * 32, p.skv);
       }
       ptx::tc_fence_before();
       __syncwarp();
