@@ -81,7 +81,7 @@ struct BLayout {
   static constexpr int kChunks = D / 64;
   static constexpr int kQStages = 2;                // Q tile + the rows' aux runs
   static constexpr int kDoStages = (D == 64) ? 2 : 1;
-  static constexpr int kStageBufs = (D == 64) ? 2 : 1;  // reduction staging boxes per warp
+  static constexpr int kStageBufs = (D == 64) ? 4 : 2;  // reduction staging boxes per warp
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTileBytes;
   static constexpr int kOffQ = 2 * kTileBytes;
@@ -89,27 +89,31 @@ struct BLayout {
   static constexpr int kOffDS = kOffDO + kDoStages * kTileBytes;  // dS, 128 keys x 128 queries bf16
   static constexpr int kOffAux = kOffDS + 2 * kChunkBytes;        // per Q stage: 128 + 128 floats
   static constexpr int kOffStage = kOffAux + kQStages * 1024;     // 4 warps x kStageBufs x 4 KB
-  static constexpr int kOffBar = kOffStage + 4 * kStageBufs * 4096;
+  static constexpr int kDataBytes = kOffStage + 4 * kStageBufs * 4096;  // from a 1024-byte boundary
   // kv_full, kv_empty, q_full[Q], q_empty[Q], do_full[DO], do_empty[DO], s_full, p_ready, dp_full,
-  // ds_ready, dq_full, dq_free, acc_full, acc_empty, drain
+  // ds_ready, dq_full, dq_free, acc_full, acc_empty, drain; then the control words
   static constexpr int kNumBars = 2 + 2 * kQStages + 2 * kDoStages + 9;
-  static constexpr int kOffCtl = kOffBar + kNumBars * 8;
-  static constexpr int kBytes = kOffCtl + 16;
-  static constexpr int kSmemLaunch = kBytes + 1024;
+  static constexpr int kOffCtl = kNumBars * 8;
+  static constexpr int kCtlBytes = 256;  // barriers + control words, placed in the alignment gap
+  // The data region starts at the first 1024-byte boundary of the dynamic window; the barriers
+  // sit in the gap before it when that gap holds them, else right after the data: either way the
+  // whole layout fits in kDataBytes + 1024 bytes whatever the window's alignment.
+  static constexpr int kSmemLaunch = kDataBytes + 1024;
   // tensor memory columns; dQ: own columns at D=64, the dP^T columns at D=128 (free once the
   // dK product has consumed dS^T, and read out before the next dP^T)
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
   static constexpr uint32_t kColDQ = (D == 64) ? 384 : 128;
 };
+static_assert(BLayout<128>::kOffCtl + 16 <= BLayout<128>::kCtlBytes, "barrier area");
 static_assert(BLayout<128>::kSmemLaunch <= 232448, "shared memory budget (D=128)");
 static_assert(BLayout<64>::kSmemLaunch <= 232448, "shared memory budget (D=64)");
 static_assert(BLayout<64>::kColDQ + 64 <= 512 && BLayout<128>::kColDK + 128 <= 512, "tensor memory budget");
 
-// Register split: 4 warps x 120 (TMA / MMA) + 4 x 248 (gradient) + 4 x 136 (reduction) =
+// Register split: 4 warps x 128 (TMA / MMA) + 4 x 248 (gradient) + 4 x 128 (reduction) =
 // 12 warps x 168, the launch's allocation.
-constexpr uint32_t kRegsControl = 120;
+constexpr uint32_t kRegsControl = 128;
 constexpr uint32_t kRegsGrad = 248;
-constexpr uint32_t kRegsRed = 136;
+constexpr uint32_t kRegsRed = 128;
 static_assert(4 * kRegsControl + 4 * kRegsGrad + 4 * kRegsRed == 12 * 168, "register split must match launch");
 
 struct Bars {
@@ -148,12 +152,7 @@ __device__ __forceinline__ uint32_t reduce_box(uint32_t stage0, int lane, uint32
   if (y >= rows) return nred;
   const uint32_t sb = stage0 + (nred % BUFS) * 4096u;
   // the reduction that used this buffer last has finished reading it
-  if (lane == 0) {
-    if (BUFS == 2)
-      ptx::bulk_wait_read_1();
-    else
-      ptx::bulk_wait_read_all();
-  }
+  if (lane == 0) ptx::bulk_wait_read<BUFS - 1>();
   __syncwarp();
   const uint32_t row = sb + static_cast<uint32_t>(lane) * 128u;
   const uint32_t sw = static_cast<uint32_t>(lane & 7);
@@ -179,17 +178,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv) {
   using L = BLayout<D>;
   using namespace sync;
-  extern __shared__ uint8_t smem_raw[];
+  extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
+  uint8_t* ctl_area = (smem - smem_raw >= L::kCtlBytes) ? smem_raw : smem + L::kDataBytes;
   const uint32_t sbase = ptx::smem_u32(smem);
+  const uint32_t cbase = ptx::smem_u32(ctl_area);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t cta = blockIdx.x;
   const int64_t grid = gridDim.x;
 
   Bars b;
-  b.kv_full = sbase + L::kOffBar;
+  b.kv_full = cbase;
   b.kv_empty = b.kv_full + 8;
   b.q_full = b.kv_empty + 8;
   b.q_empty = b.q_full + 8 * L::kQStages;
@@ -204,8 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   b.acc_full = b.dq_free + 8;
   b.acc_empty = b.acc_full + 8;
   b.drain = b.acc_empty + 8;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffCtl);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffCtl + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl_area + L::kOffCtl);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctl_area + L::kOffCtl + 4);
   const Ctl ctl{abort_flag, p.status, p.timeout_ns};
 
   if (threadIdx.x == 0) {
