@@ -44,10 +44,16 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "sync.cuh"
 
 namespace cpattn {
 
 namespace {
+
+using sync::Ctl;
+using sync::unit_of;
+using sync::wait_drain;
+using sync::wait_warp;
 
 constexpr int kRows = 128;     // rows per Q tile
 constexpr int kKeys = 128;     // keys per KV tile
@@ -135,48 +141,6 @@ struct Bars {
   uint32_t never, drain;
 };
 
-struct Ctl {
-  volatile int* abort;
-  int32_t* status;
-  int64_t timeout_ns;
-};
-
-__device__ __forceinline__ void raise_abort(const Ctl& c, int site) {
-  *c.abort = 1;
-  if (c.status != nullptr) atomicCAS(c.status, 0, CP_ERR_TIMEOUT | (site << 8));
-}
-
-// Waits for phase `parity` of `bar`; gives up (returns false) when the kernel is aborting or
-// when the wait exceeds the time limit, in which case it starts the abort itself.
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Ctl& c, int site) {
-  if (ptx::mbar_test_wait(bar, parity)) return true;
-  const uint64_t t0 = ptx::globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if ((it & 31u) == 0) {
-      if (*c.abort) return false;
-      if (static_cast<int64_t>(ptx::globaltimer() - t0) > c.timeout_ns) {
-        raise_abort(c, site);
-        return false;
-      }
-    }
-  }
-}
-
-// Every lane of the warp waits; the outcome is the same for the whole warp.
-__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const Ctl& c, int site) {
-  const bool ok = wait_bounded(bar, parity, c, site);
-  return __all_sync(0xffffffffu, ok);
-}
-
-// Teardown wait: ignores the abort flag (the copy or MMA must really finish) but stays bounded.
-__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, int64_t timeout_ns) {
-  const uint64_t t0 = ptx::globaltimer();
-  while (!ptx::mbar_try_wait(bar, parity)) {
-    if (static_cast<int64_t>(ptx::globaltimer() - t0) > timeout_ns) return;
-  }
-}
-
 // Keys of chunk c that query `row` may see: all of them when not causal, else the keys j with
 // base + stride * j <= q_pos(row) (positions grow with the index, so they are a prefix).
 template <int MAXC>
@@ -188,11 +152,6 @@ __device__ __forceinline__ int64_t visible_keys(const TcParams& p, const ChunkTa
   if (qp < ch.base[c]) return 0;
   const int64_t n = (qp - ch.base[c]) / ch.stride[c] + 1;
   return n < skv ? n : skv;
-}
-
-// The k-th unit of CTA b: rounds of `grid` units, forward on even rounds, backward on odd ones.
-__device__ __forceinline__ int64_t unit_of(int64_t k, int64_t b, int64_t grid) {
-  return k * grid + ((k & 1) ? (grid - 1 - b) : b);
 }
 
 struct Unit {
@@ -713,41 +672,11 @@ __global__ void fill_empty_kernel(void* o, int o_bf16, float* lse, int64_t rows,
   }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
-
 // 2-D map over a token-major tensor viewed as [tokens, heads*d]; box = 128 bytes of columns x
-// 128 rows with 128-byte swizzle (for bf16 operands: the canonical K-major / MN-major UMMA
-// layout; for the output: the staging layout of the epilogue).
+// 128 rows with 128-byte swizzle (bf16 operands: the canonical K-major / MN-major UMMA layout;
+// the output: the staging layout of the epilogue).
 bool make_map(CUtensorMap* m, const void* base, int64_t tokens, int64_t row_elems, bool fp32 = false) {
-  EncodeTiledFn enc = get_encode_fn();
-  if (enc == nullptr) return false;
-  const int64_t es = fp32 ? 4 : 2;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_elems), static_cast<cuuint64_t>(tokens)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_elems * es)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / es), 128};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return encode_map_2d(m, base, tokens, row_elems, fp32, 128);
 }
 
 template <int D, int MAXC>
