@@ -344,6 +344,70 @@ class BwdStep:
         return len(self.preps) + len(self.calls)
 
 
+class UlyssesBwdStep:
+    """Backward of the Ulysses workload: the forward's three exchanges in reverse ([Halo]) -- dO
+    seq->head, per head-rank prep and full-sequence partial backward, dQ and fused dK|dV
+    head->seq in fp32.  The forward step runs once first (head-sharded O and LSE)."""
+
+    def __init__(self, fwd, seed=4343):
+        import context_blockwise_attention_gb300 as cpa
+        from context_blockwise_attention_gb300 import workloads as wl
+        self.cpa = cpa
+        w = self.w = fwd.w
+        dev = fwd.device
+        cp, S = w.cp, w.seq_len
+        fwd.run()
+        torch.cuda.synchronize()
+        self.fwd = fwd
+        hl, kl = w.hq // cp, w.hkv // cp
+        self.xdo = [wl.normal((S // cp, w.hq, w.d), torch.bfloat16, seed + r, 1.0, device=dev) for r in range(cp)]
+        self.ydo = [torch.empty((S, hl, w.d), dtype=torch.bfloat16, device=dev) for _ in range(cp)]
+        self.aux = [torch.empty(cpa.bwd_aux_floats(S, hl), dtype=torch.float32, device=dev) for _ in range(cp)]
+        self.dqh = [torch.zeros((S, hl, w.d), device=dev) for _ in range(cp)]
+        self.dkh = [torch.zeros((S, kl, w.d), device=dev) for _ in range(cp)]
+        self.dvh = [torch.zeros((S, kl, w.d), device=dev) for _ in range(cp)]
+        self.dqs = [torch.empty((S // cp, w.hq, w.d), device=dev) for _ in range(cp)]
+        self.dks = [torch.empty((S // cp, w.hkv, w.d), device=dev) for _ in range(cp)]
+        self.dvs = [torch.empty((S // cp, w.hkv, w.d), device=dev) for _ in range(cp)]
+        full = cpa.PosMap(0, 1)
+        self.flops = cp * 10 * w.d * hl * cpa.visible_pairs(full, S, full, S, True)
+        # reshard bytes: dO (bf16) in, dQ and dK|dV (fp32) out; one read and one write each
+        self.reshard_bytes = 2 * S * w.d * (w.hq * 2 + (w.hq + 2 * w.hkv) * 4)
+
+    def run(self, timers=None, rtimers=None):
+        cpa, w = self.cpa, self.w
+        cp, S = w.cp, w.seq_len
+        stream = torch.cuda.current_stream()
+
+        def ev():
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(stream)
+            return e
+        for t in self.dqh + self.dkh + self.dvh:
+            t.zero_()
+        t0 = ev() if rtimers is not None else None
+        cpa.ulysses_reshard("seq_to_head", [self.xdo], cp, S, w.layout, out=[self.ydo])
+        t1 = ev() if rtimers is not None else None
+        full = cpa.PosMap(0, 1)
+        f = self.fwd
+        for r in range(cp):
+            cpa.attn_bwd_prep(f.yo[r], self.ydo[r], f.ylse[r], aux=self.aux[r])
+        a = ev() if timers is not None else None
+        for r in range(cp):
+            cpa.partial_attn_bwd(f.yq[r], f.yk[r], f.yv[r], self.ydo[r], self.aux[r], full, full,
+                                 self.dqh[r], self.dkh[r], self.dvh[r])
+        b = ev() if timers is not None else None
+        cpa.ulysses_reshard("head_to_seq", [self.dqh], cp, S, w.layout, out=[self.dqs])
+        cpa.ulysses_reshard("head_to_seq", [self.dkh, self.dvh], cp, S, w.layout, out=[self.dks, self.dvs])
+        t2 = ev() if rtimers is not None else None
+        if timers is not None:
+            timers.append((a, b))
+        if rtimers is not None:
+            rtimers.append((t0, t1))
+            rtimers.append((b, t2))
+        return 3 + 2 * cp
+
+
 # ----------------------------------------------------------------------------- measurement
 
 def aggregate(total_ms_local, flops_local, steps, world, device=None):
@@ -670,19 +734,22 @@ def run_gpu(args):
                  "path": "one cp_partial_attn_chunks per query block (no partials, no merge)"}
         del fstep
     backward = None
-    if args.config != 4 and w.dtype == "bf16" and not args.no_backward:
+    if w.dtype == "bf16" and not args.no_backward:
         # the backward of the same workload (f4), timed the same way (L2 flushed per step)
-        bstep = BwdStep(Step(args.config, dev, query_rank=qr, layout=layout, fused=True))
+        if args.config == 4:
+            bstep = UlyssesBwdStep(Step(4, dev))
+        else:
+            bstep = BwdStep(Step(args.config, dev, query_rank=qr, layout=layout, fused=True))
         for _ in range(args.warmup):
             bstep.run()
         barrier()
-        bms, btimes, blaunch = [], [], 0
+        bms, btimes, rtimes, blaunch = [], [], [], 0
         for _ in range(args.steps):
             flush.zero_()
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            blaunch += bstep.run(btimes)
+            blaunch += bstep.run(btimes, rtimes) if args.config == 4 else bstep.run(btimes)
             b.record(stream)
             torch.cuda.synchronize()
             bms.append(a.elapsed_time(b))
@@ -695,8 +762,15 @@ def run_gpu(args):
                     "kernel": "attn_bwd_tc_kernel", "kernel_ms_per_step": b_kernel_ms,
                     "achieved": b_ach, "peak": peaks["bf16"], "frac": b_ach / peaks["bf16"],
                     "launches_per_step": blaunch // args.steps,
-                    "path": "prep per query block + one cp_partial_attn_bwd per (block, chunk); "
-                            "dK/dV accumulated into the chunk owners' shards; gradients zeroed in the step"}
+                    "path": ("dO seq->head, per head-rank prep + full-sequence cp_partial_attn_bwd, "
+                             "dQ and dK|dV head->seq (fp32); gradients zeroed in the step")
+                    if args.config == 4 else
+                    ("prep per query block + one cp_partial_attn_bwd per (block, chunk); "
+                     "dK/dV accumulated into the chunk owners' shards; gradients zeroed in the step")}
+        if rtimes:
+            r_ms = sum(s_.elapsed_time(e_) for s_, e_ in rtimes) / args.steps
+            gbs = bstep.reshard_bytes / (r_ms * 1e-3) / 1e9
+            backward["reshard"] = {"ms": r_ms, "GB/s": gbs, "frac": gbs / peaks["hbm"], "bytes": bstep.reshard_bytes}
         del bstep
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

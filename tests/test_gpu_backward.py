@@ -220,3 +220,42 @@ def test_end_to_end_forward_then_backward():
     for c, (dk, dv) in enumerate(grads):
         compare_grad(dk.cpu().numpy(), dk_ref[c * n:(c + 1) * n], TOL_GRAD_BF16, f"e2e dK chunk {c}")
         compare_grad(dv.cpu().numpy(), dv_ref[c * n:(c + 1) * n], TOL_GRAD_BF16, f"e2e dV chunk {c}")
+
+
+def test_ulysses_backward_three_steps_in_reverse():
+    # Ulysses: forward = reshard Q and K|V seq->head, full-sequence attention per head-rank,
+    # reshard O head->seq; backward = the same three steps in reverse: dO seq->head, the
+    # backward per head-rank, dQ and dK|dV head->seq (fp32).  Compared with the gradients of
+    # unsharded attention.
+    seq, cp, hq, hkv, d = 1024, 4, 8, 4, 64
+    full = PosMap(0, 1)
+    qf = wl.normal((seq, hq, d), torch.bfloat16, 81, 0.5)
+    kf = wl.normal((seq, hkv, d), torch.bfloat16, 82, 0.5)
+    vf = wl.normal((seq, hkv, d), torch.bfloat16, 83, 1.0)
+    dof = wl.normal((seq, hq, d), torch.bfloat16, 84, 1.0)
+    local = seq // cp
+    shard = lambda x: [x[r * local:(r + 1) * local].contiguous().to(DEV) for r in range(cp)]  # noqa: E731
+    (yq,) = cpa.ulysses_reshard("seq_to_head", [shard(qf)], cp, seq)
+    yk, yv = cpa.ulysses_reshard("seq_to_head", [shard(kf), shard(vf)], cp, seq)
+    (ydo,) = cpa.ulysses_reshard("seq_to_head", [shard(dof)], cp, seq)
+    dqh, dkh, dvh = [], [], []
+    for r in range(cp):
+        o, lse = cpa.partial_attn(yq[r], yk[r], yv[r], full, full, o_dtype=torch.bfloat16)
+        aux = cpa.attn_bwd_prep(o, ydo[r], lse)
+        dq = torch.zeros(yq[r].shape, device=DEV)
+        dk = torch.zeros(yk[r].shape, device=DEV)
+        dv = torch.zeros(yv[r].shape, device=DEV)
+        cpa.partial_attn_bwd(yq[r], yk[r], yv[r], ydo[r], aux, full, full, dq, dk, dv)
+        dqh.append(dq)
+        dkh.append(dk)
+        dvh.append(dv)
+    (dqs,) = cpa.ulysses_reshard("head_to_seq", [dqh], cp, seq)
+    dks, dvs = cpa.ulysses_reshard("head_to_seq", [dkh, dvh], cp, seq)
+    torch.cuda.synchronize()
+    pos = np.arange(seq)
+    dq_ref, dk_ref, dv_ref = oracle.attention_backward(qf, kf, vf, dof, pos, pos, causal=True)
+    for r in range(cp):
+        sl = slice(r * local, (r + 1) * local)
+        compare_grad(dqs[r].cpu().numpy(), dq_ref[sl], TOL_GRAD_BF16, f"Ulysses dQ shard {r}")
+        compare_grad(dks[r].cpu().numpy(), dk_ref[sl], TOL_GRAD_BF16, f"Ulysses dK shard {r}")
+        compare_grad(dvs[r].cpu().numpy(), dv_ref[sl], TOL_GRAD_BF16, f"Ulysses dV shard {r}")
