@@ -579,7 +579,7 @@ def run_reference(args):
     w = wl.WORKLOADS[args.config]
     if world > 1 and rank != 0:
         return
-    rows = args.ref_rows
+    rows = args.ref_rows or 64
     for _ in range(args.warmup):
         oracle_sample(args.config, max(1, rows // 4), layout=args.layout)
     times, fl = [], 0
@@ -774,12 +774,23 @@ def run_gpu(args):
         del bstep
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        t, fl, desc = oracle_sample(args.config, args.ref_rows, layout=layout)
+        if args.ref_rows:
+            t, fl, desc = oracle_sample(args.config, args.ref_rows, layout=layout)
+        else:
+            # about 10 s of oracle work: time 16 rows, then size the sample from that rate
+            t16, _, _ = oracle_sample(args.config, 16, layout=layout)
+            rows = int(min(max(16, 16 * 10.0 / max(t16, 1e-3)), w.local_len if args.config != 4 else w.seq_len))
+            t, fl, desc = oracle_sample(args.config, rows, layout=layout)
         cpu = {"value": fl / t / 1e12, "unit": "TFLOP/s", "cores": _blas_threads(),
-               "kind": "oracle", "sample": desc, "seconds": t}
+               "kind": "oracle", "sample": desc, "seconds": t,
+               # 4*D*Hq flops per visible pair: the sample's rate in pairs/s, and the whole
+               # workload's time at that rate (extrapolated, not measured)
+               "pairs_per_s": fl / (4 * w.d * (w.hq // (w.cp if args.config == 4 else 1))) / t,
+               "extrapolated_full_workload_s": step.flops / (fl / t)}
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+                "ms_median": float(np.median(step_ms)), "ms_best": float(min(step_ms)),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16" if w.dtype == "bf16" else "f32",
                 "data": "synthetic (seeded N(0,1) inputs; no dataset or weights)",
@@ -949,7 +960,9 @@ def main():
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--layout", default=None, choices=[None, "contiguous", "strided", "two_block"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--ref-rows", type=int, default=64)
+    ap.add_argument("--ref-rows", type=int, default=0,
+                    help="oracle sample rows (0: about 10 s of oracle work for the cpu baseline, "
+                         "64 per step for --impl reference)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fused", action="store_true",
                     help="skip the extra measurement of the fused chunk-list path")

@@ -326,7 +326,7 @@ def attn_bwd_prep(o, d_o, lse, aux=None, stream=None):
 
 
 def partial_attn_bwd(q, k, v, d_o, aux, q_pos: PosMap, kv_pos: PosMap, dq, dk, dv, causal=True,
-                     scale=0.0, status=None, wait_timeout_ms=0, stream=None):
+                     scale=0.0, status=None, wait_timeout_ms=0, flags=0, stream=None):
     """Adds one (query shard, KV chunk) pair's share of the attention gradients into ``dq``
     [Sq, Hq, D] and ``dk``, ``dv`` [Skv, Hkv, D] (fp32, accumulated in place)."""
     lib = load_library()
@@ -362,6 +362,7 @@ def partial_attn_bwd(q, k, v, d_o, aux, q_pos: PosMap, kv_pos: PosMap, dq, dk, d
             raise CpError(CP_ERR_INVALID_ARG, "status must be int32")
         desc.status = status.data_ptr()
     desc.wait_timeout_ms = int(wait_timeout_ms)
+    desc.flags = int(flags)
     _check(lib.cp_partial_attn_bwd(ctypes.byref(desc), _stream(stream)))
     return dq, dk, dv
 

@@ -60,6 +60,7 @@ enum BwdSite : int {
   kSAccEmpty = 12,
   kSDoFull = 13,
   kSDoEmpty = 14,
+  kSTest = 15,
 };
 
 struct BwdParams {
@@ -72,6 +73,7 @@ struct BwdParams {
   float scale, sl2;    // scale, scale * log2(e)
   int64_t q_base, q_stride, k_base, k_stride;
   int64_t timeout_ns;
+  int32_t test_stall;  // test only: block 0's MMA warp first waits on a barrier nothing completes
 };
 
 template <int D>
@@ -91,8 +93,8 @@ struct BLayout {
   static constexpr int kOffStage = kOffAux + kQStages * 1024;     // 4 warps x kStageBufs x 4 KB
   static constexpr int kDataBytes = kOffStage + 4 * kStageBufs * 4096;  // from a 1024-byte boundary
   // kv_full, kv_empty, q_full[Q], q_empty[Q], do_full[DO], do_empty[DO], s_full, p_ready, dp_full,
-  // ds_ready, dq_full, dq_free, acc_full, acc_empty, drain; then the control words
-  static constexpr int kNumBars = 2 + 2 * kQStages + 2 * kDoStages + 9;
+  // ds_ready, dq_full, dq_free, acc_full, acc_empty, drain, never; then the control words
+  static constexpr int kNumBars = 2 + 2 * kQStages + 2 * kDoStages + 10;
   static constexpr int kOffCtl = kNumBars * 8;
   static constexpr int kCtlBytes = 256;  // barriers + control words, placed in the alignment gap
   // The data region starts at the first 1024-byte boundary of the dynamic window; the barriers
@@ -118,7 +120,7 @@ static_assert(4 * kRegsControl + 4 * kRegsGrad + 4 * kRegsRed == 12 * 168, "regi
 
 struct Bars {
   uint32_t kv_full, kv_empty, q_full, q_empty, do_full, do_empty;  // q_*, do_*: stage 0, +8 per stage
-  uint32_t s_full, p_ready, dp_full, ds_ready, dq_full, dq_free, acc_full, acc_empty, drain;
+  uint32_t s_full, p_ready, dp_full, ds_ready, dq_full, dq_free, acc_full, acc_empty, drain, never;
 };
 
 struct BUnit {
@@ -205,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   b.acc_full = b.dq_free + 8;
   b.acc_empty = b.acc_full + 8;
   b.drain = b.acc_empty + 8;
+  b.never = b.drain + 8;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl_area + L::kOffCtl);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctl_area + L::kOffCtl + 4);
   const Ctl ctl{abort_flag, p.status, p.timeout_ns};
@@ -230,6 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(b.acc_full, 1);
     ptx::mbar_init(b.acc_empty, 4);
     ptx::mbar_init(b.drain, 1);
+    ptx::mbar_init(b.never, 1);
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
@@ -379,6 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       int64_t gi = 0, ku = 0;
       bool ok = true;
+      if (p.test_stall && blockIdx.x == 0) ok = wait_warp(b.never, 0, ctl, kSTest);
       for (int64_t k = 0; ok; ++k) {
         const int64_t u = unit_of(k, cta, grid);
         if (u >= p.n_units) break;
@@ -679,6 +684,7 @@ cp_status launch_partial_attn_bwd_tc(const cp_attn_bwd_desc& d, float scale, int
   p.k_base = d.kv_pos.base;
   p.k_stride = d.kv_pos.stride;
   p.timeout_ns = timeout_ns;
+  p.test_stall = (d.flags & CP_FLAG_TEST_STALL) ? 1 : 0;
   const int64_t grid = p.n_units < num_sms ? p.n_units : num_sms;
   if (d.d == 64) return launch_bwd_d<64>(p, d, grid, s);
   return launch_bwd_d<128>(p, d, grid, s);

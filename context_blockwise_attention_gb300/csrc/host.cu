@@ -302,7 +302,9 @@ CP_API cp_status cp_partial_attn_bwd(const cp_attn_bwd_desc* desc, cudaStream_t 
       double(d.kv_pos.base) + double(d.kv_pos.stride) * double(d.skv) > 2.0e9)
     CP_INVALID("partial attention backward: global positions exceed 2e9");
   if (!(d.scale >= 0.0f) || isinf(d.scale)) CP_INVALID("partial attention backward: scale must be finite and >= 0");
-  if (d.flags != 0) CP_INVALID("partial attention backward: unknown flag bits 0x%x", d.flags);
+  if (d.flags & ~CP_FLAG_TEST_STALL) CP_INVALID("partial attention backward: unknown flag bits 0x%x", d.flags);
+  if ((d.flags & CP_FLAG_TEST_STALL) && d.in_dtype != CP_BF16)
+    CP_INVALID("partial attention backward: CP_FLAG_TEST_STALL applies to the bf16 (tensor-core) path only");
   if (d.wait_timeout_ms < 0) CP_INVALID("partial attention backward: wait_timeout_ms must be >= 0");
   if (d.sq == 0 || d.skv == 0) return CP_OK;  // nothing to add
   if (d.q == nullptr || d.k == nullptr || d.v == nullptr || d.d_o == nullptr || d.aux == nullptr ||

@@ -284,6 +284,7 @@ cp_status cp_attn_bwd_prep(const void* o, int32_t o_dtype, const void* d_o, int3
  *   aux       the shard's cp_attn_bwd_prep output
  *   dq, dk, dv  device fp32, 16-byte aligned
  *   status, wait_timeout_ms  as cp_attn_desc (bounded in-kernel waits of the tensor-core path)
+ *   flags     0, or CP_FLAG_TEST_STALL (bf16 only; same meaning as for cp_attn_desc)
  * Within one call dq, dk, dv are updated with atomic reductions (bf16 path) or by exclusive
  * owners (fp32 path); calls on one stream follow stream order.  The summation order of dq and
  * of a GQA group's dk, dv is not fixed on the bf16 path.

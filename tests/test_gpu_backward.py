@@ -7,6 +7,8 @@ forward on the GPU too.  Gradient buffers are poisoned with a known value first:
 ACCUMULATE, so what they add is read as the difference.
 """
 
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -259,3 +261,28 @@ def test_ulysses_backward_three_steps_in_reverse():
         compare_grad(dqs[r].cpu().numpy(), dq_ref[sl], TOL_GRAD_BF16, f"Ulysses dQ shard {r}")
         compare_grad(dks[r].cpu().numpy(), dk_ref[sl], TOL_GRAD_BF16, f"Ulysses dK shard {r}")
         compare_grad(dvs[r].cpu().numpy(), dv_ref[sl], TOL_GRAD_BF16, f"Ulysses dV shard {r}")
+
+
+def test_bwd_bounded_wait_reports_timeout_and_context_survives():
+    # block 0's MMA warp waits on a barrier nothing completes: its bounded wait expires, the
+    # kernel records CP_ERR_TIMEOUT with the site, every CTA leaves, and the next call is correct
+    sq, skv, hq, hkv, d = 512, 512, 4, 2, 128
+    qm = km = PosMap(0, 1)
+    q, k, v, d_o, o32, l32 = _case_inputs(sq, skv, hq, hkv, d, True, qm, km, torch.bfloat16, 9)
+    aux = cpa.attn_bwd_prep(o32.to(DEV), d_o, l32.to(DEV))
+    dq = torch.zeros(q.shape, device=DEV)
+    dk = torch.zeros(k.shape, device=DEV)
+    dv = torch.zeros(v.shape, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    t0 = time.time()
+    cpa.partial_attn_bwd(q, k, v, d_o, aux, qm, km, dq, dk, dv, status=status, wait_timeout_ms=200,
+                         flags=cpa.api.CP_FLAG_TEST_STALL)
+    torch.cuda.synchronize()
+    assert time.time() - t0 < 20
+    st = int(status.item())
+    assert st & 0xff == cpa.api.CP_ERR_TIMEOUT and (st >> 8) >= 1, hex(st)
+    got = _run_bwd(q, k, v, d_o, o32, l32, qm, km, True)
+    ref = _oracle_bwd(q, k, v, d_o, o32, l32, qm, km, True)
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        compare_grad(g, r, TOL_GRAD_BF16, f"{name} after a timed-out call")
+

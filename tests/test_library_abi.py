@@ -230,7 +230,7 @@ def _bwd_desc(**kw):
 
 @pytest.mark.parametrize("field,value", [
     ("d", 96), ("hq", 5), ("hkv", 0), ("in_dtype", 4), ("causal", 3), ("q", 0), ("aux", 0),
-    ("dq", 0), ("dk", 0x2004), ("sq", -1), ("skv", -2), ("flags", 1),
+    ("dq", 0), ("dk", 0x2004), ("sq", -1), ("skv", -2), ("flags", 1), ("flags", 0x200),
     ("q_pos", api._PosMap(0, 0)), ("kv_pos", api._PosMap(-1, 1)), ("scale", float("inf")),
     ("wait_timeout_ms", -1),
 ])
@@ -252,3 +252,10 @@ def test_bwd_prep_rejects():
     assert lib.cp_attn_bwd_prep(p, 0, p, 1, p, 16, 2, 64, ctypes.c_void_p(0x1004), None) == \
         api.CP_ERR_INVALID_ARG  # aux alignment
     assert cpa.bwd_aux_floats(130, 3) == 2 * 3 * 256
+
+
+def test_bwd_test_stall_needs_bf16():
+    lib = cpa.load_library()
+    d = _bwd_desc(flags=api.CP_FLAG_TEST_STALL, in_dtype=api.CP_F32)
+    assert lib.cp_partial_attn_bwd(ctypes.byref(d), None) == api.CP_ERR_INVALID_ARG
+
