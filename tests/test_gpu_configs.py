@@ -238,3 +238,44 @@ def test_cfg2_backward_sampled():
         compare_grad(bstep.dk[r].cpu().numpy()[keys], dk_ref, TOL_GRAD_BF16, f"cfg2 dK shard {r} (sampled keys)")
         compare_grad(bstep.dv[r].cpu().numpy()[keys], dv_ref, TOL_GRAD_BF16, f"cfg2 dV shard {r} (sampled keys)")
 
+
+
+def test_cfg4_backward_sampled():
+    # the Ulysses backward at full size as the bench times it (dO seq->head, 4 head-rank backward
+    # calls over the whole sequence, dQ and dK|dV head->seq).  dQ exact on sampled rows (the
+    # oracle computes the rows' O and LSE itself); dK, dV through identities of the softmax
+    # Jacobian that hold at any size: per KV head, sum_j dV_j = sum_i (group's dO_i) and
+    # sum_j dK_j = 0
+    w = wl.WORKLOADS[4]
+    cp, S = w.cp, w.seq_len
+    hl, kl = w.hq // cp, w.hkv // cp
+    bstep = bench.UlyssesBwdStep(bench.Step(4, DEV))
+    bstep.run()
+    torch.cuda.synchronize()
+    f = bstep.fwd
+    q_full = torch.cat([x.cpu() for x in f.qs])  # contiguous layout: global order
+    k_full = torch.cat([x.cpu() for x in f.ks])
+    v_full = torch.cat([x.cpu() for x in f.vs])
+    do_full = torch.cat([x.cpu() for x in bstep.xdo])
+    dq = torch.cat([x.cpu() for x in bstep.dqs]).numpy()
+    dk = torch.cat([x.cpu() for x in bstep.dks]).double().numpy()
+    dv = torch.cat([x.cpu() for x in bstep.dvs]).double().numpy()
+    gpos = np.arange(S)
+    rows = wl.sample_rows(S, 48, seed=6, must=[0, 1, 128, S - 1])
+    ri = torch.from_numpy(rows)
+    for r in range(cp):
+        qh = q_full[:, r * hl:(r + 1) * hl]
+        kh = k_full[:, r * kl:(r + 1) * kl]
+        vh = v_full[:, r * kl:(r + 1) * kl]
+        doh = do_full[:, r * hl:(r + 1) * hl]
+        o_ref, l_ref = oracle.attention(qh[ri], kh, vh, rows, gpos, causal=True)
+        dq_ref = oracle.chunk_backward(qh[ri], kh, vh, doh[ri], o_ref, l_ref, rows, gpos, causal=True)[0]
+        compare_grad(dq[rows][:, r * hl:(r + 1) * hl], dq_ref, TOL_GRAD_BF16, f"cfg4 dQ head-rank {r}")
+    group = w.hq // w.hkv
+    do64 = do_full.double().numpy()
+    for g in range(w.hkv):
+        want = do64[:, g * group:(g + 1) * group].sum(axis=(0, 1))
+        got = dv[:, g].sum(axis=0)
+        assert np.abs(got - want).max() <= 1e-2 * max(1.0, np.abs(want).max()), f"cfg4 sum dV, KV head {g}"
+        ksum = np.abs(dk[:, g].sum(axis=0)).max()
+        assert ksum <= 1e-2 * max(1.0, np.abs(dk[:, g]).sum(axis=0).max()), f"cfg4 sum dK, KV head {g}"
