@@ -680,12 +680,23 @@ def run_gpu(args):
     achieved = step.flops / (attn_ms * 1e-3) / 1e12
     traffic = _profile_traffic(os.path.join(ROOT, "context_blockwise_attention_gb300", "csrc",
                                             "attn_tc.cu"), f"cfg{args.config}")
-    roofline = {"bound": "tensor", "kernel": "attn_tc_kernel", "achieved": achieved,
-                "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16"],
-                "peak_source": f"{peaks['source']} bf16 dense (burst)",
-                "frac_of_sustained": achieved / peaks["bf16_sustained"],
-                "launches_per_step": n_attn,
-                "traffic": traffic}
+    if w.dtype == "f32":
+        # fp32 inputs run on CUDA cores (FFMA): the peak is SMs x 128 FMA lanes x 2 flops x the
+        # maximum SM clock (no measured FFMA peak exists for this machine)
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        mhz = clocks.get("sm_max_mhz") or 2070.0
+        ffma_peak = sms * 128 * 2 * mhz * 1e6 / 1e12
+        roofline = {"bound": "alu", "kernel": "attn_simt_kernel", "achieved": achieved, "peak": ffma_peak,
+                    "unit": "TFLOP/s", "frac": achieved / ffma_peak,
+                    "peak_source": f"derived: {sms} SMs x 128 FFMA/clk x 2 x {mhz:.0f} MHz",
+                    "launches_per_step": n_attn, "traffic": None}
+    else:
+        roofline = {"bound": "tensor", "kernel": "attn_tc_kernel", "achieved": achieved,
+                    "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16"],
+                    "peak_source": f"{peaks['source']} bf16 dense (burst)",
+                    "frac_of_sustained": achieved / peaks["bf16_sustained"],
+                    "launches_per_step": n_attn,
+                    "traffic": traffic}
     extra = {"attn_ms_per_step": attn_ms, "attn_tflops": achieved,
              "step_flop": step.flops, "query_rank": qr}
     if timers.get("rank_attn"):
