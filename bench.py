@@ -206,8 +206,9 @@ class Step:
         self.pos_bufs = []
 
     # ----------------------------------------------------------------- launch sequence
-    def run(self, timers=None):
-        """Launch one step on the current stream; optional timers record per-kernel events."""
+    def run(self, timers=None, chunk_ready=None):
+        """Launch one step on the current stream; optional timers record per-kernel events;
+        `chunk_ready` maps a source rank to an event each of its partials waits for first."""
         cpa, w = self.cpa, self.w
         stream = torch.cuda.current_stream()
         n = 0
@@ -249,10 +250,14 @@ class Step:
         # with timers["rank_attn"], an event at every change of query rank gives each simulated
         # rank's own attention time
         per_rank = timers is not None and "rank_attn" in timers
-        launches = [(m[0], cpa.partial_attn, kw) for kw, m in zip(self.attn_calls, self.call_meta)]
-        launches += [(qr, cpa.partial_attn_chunks, kw) for kw, qr in zip(self.fused_calls, self.fused_meta)]
+        launches = [(m[0], cpa.partial_attn, kw, m[3]) for kw, m in zip(self.attn_calls, self.call_meta)]
+        launches += [(qr, cpa.partial_attn_chunks, kw, None) for kw, qr in zip(self.fused_calls, self.fused_meta)]
         cur, start = None, None
-        for qr, fn, kw in launches:
+        waited = set()
+        for qr, fn, kw, src in launches:
+            if chunk_ready is not None and src is not None and src not in waited:
+                stream.wait_event(chunk_ready[src])
+                waited.add(src)
             if per_rank and qr != cur:
                 e = ev()
                 if cur is not None:
@@ -273,10 +278,43 @@ class Step:
         return n
 
     def run_e2e(self):
-        """Host -> device copies of the inputs, the step, device -> host copies of the outputs."""
-        for h, d in self.host_inputs:
-            d.copy_(h, non_blocking=True)
-        n = self.run()
+        """Host -> device copies of the inputs, the step, device -> host copies of the outputs.
+
+        Per-chunk path: the copies run on a second stream -- the query shards first, then each
+        source rank's K and V in the order the step first uses them -- and each partial waits
+        only for its own chunk's copy (chunks arriving while earlier ones are computed, the FCP
+        article's section 4.3); same launches, same result.  Other paths copy everything first."""
+        if self.cfg == 4 or self.fused or not self.attn_calls:
+            for h, d in self.host_inputs:
+                d.copy_(h, non_blocking=True)
+            n = self.run()
+        else:
+            compute = torch.cuda.current_stream()
+            if getattr(self, "_copy_stream", None) is None:
+                self._copy_stream = torch.cuda.Stream()
+            copy = self._copy_stream
+            copy.wait_stream(compute)  # the device buffers are free once the previous step is done
+            host_of = {id(d): h for h, d in self.host_inputs}
+            order = []
+            for m in self.call_meta:
+                if m[3] not in order:
+                    order.append(m[3])
+            events = {}
+            with torch.cuda.stream(copy):
+                for _, q, _, _ in self.rank_plans:
+                    q.copy_(host_of[id(q)], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(copy)
+                events["q"] = e
+                for src in order:
+                    k, v = self.kv[src]
+                    k.copy_(host_of[id(k)], non_blocking=True)
+                    v.copy_(host_of[id(v)], non_blocking=True)
+                    e = torch.cuda.Event()
+                    e.record(copy)
+                    events[src] = e
+            compute.wait_event(events["q"])
+            n = self.run(chunk_ready=events)
         for d, h in self.host_outputs:
             h.copy_(d, non_blocking=True)
         return n
