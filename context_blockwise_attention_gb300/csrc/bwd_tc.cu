@@ -21,7 +21,11 @@
 //     concurrent CTAs and GQA heads accumulate without a separate pass.
 //   * Tensor memory: S^T (128 fp32 columns, P^T bf16 written over its first 64), dP^T (128,
 //     dS^T bf16 over its first 64), dV and dK accumulators (D each), dQ (D; for D = 128 it
-//     reuses the S^T columns once the dV product has consumed P^T).
+//     reuses the dP^T columns once the dK product has consumed dS^T).
+//   * Issue order per query tile g: dP^T(g), dV(g), then S^T(g+1) of the same unit -- so the
+//     gradient warps start P^T(g+1) as soon as dS^T(g) is done, while dK(g) and dQ(g) run --
+//     then dK(g), dQ(g).  Q tiles (with the rows' aux runs) have two stages, dO a ring of one
+//     (D = 128) or two (D = 64) stages.
 //   * The five products: S^T and dP^T are K-major x K-major from shared memory; dV and dK take
 //     P^T / dS^T straight from tensor memory with dO / Q as MN-major B operands; dQ takes dS from
 //     shared memory as an MN-major A operand (the gradient warps write it there in the 128-byte
