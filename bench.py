@@ -330,12 +330,13 @@ class Step:
 
 class BwdStep:
     """Backward of a step's attention: per query block the prep kernel (from the
-    block's final O and LSE, produced by running `fwd` once), then one partial backward per
-    (query block, visible chunk) pair in arrival order; dQ accumulates per block, dK and dV into
-    the chunk owner's shard buffers (the pages' reduce-scatter).  Gradients are zeroed inside the
-    step, as a training step would."""
+    block's final O and LSE, produced by running `fwd` once), then the partial backward of every
+    (query block, visible chunk) pair -- one chunk-list call per block (`fused`, default) or one
+    call per pair in arrival order; dQ accumulates per block, dK and dV into the chunk owner's
+    shard buffers (the pages' reduce-scatter).  Gradients are zeroed inside the step, as a
+    training step would."""
 
-    def __init__(self, fwd, seed=4242):
+    def __init__(self, fwd, seed=4242, fused=True):
         import context_blockwise_attention_gb300 as cpa
         from context_blockwise_attention_gb300 import workloads as wl
         self.cpa = cpa
@@ -356,13 +357,20 @@ class BwdStep:
             dq = torch.zeros(tuple(qb.shape), dtype=torch.float32, device=dev)
             self.dqs.append(dq)
             self.preps.append(dict(o=ob, d_o=d_o, lse=lb, aux=aux))
+            clist = []
             for src, lo, nk, kmap in chunks:
                 k, v = fwd.kv[src]
-                self.calls.append(dict(q=qb, k=k[lo:lo + nk], v=v[lo:lo + nk], d_o=d_o, aux=aux, q_pos=qmap,
-                                       kv_pos=kmap, dq=dq, dk=self.dk[src][lo:lo + nk],
-                                       dv=self.dv[src][lo:lo + nk], causal=w.causal))
+                clist.append((k[lo:lo + nk], v[lo:lo + nk], kmap, self.dk[src][lo:lo + nk], self.dv[src][lo:lo + nk]))
                 # five products of 2*D flops per visible pair: S, dP, dV, dK, dQ
                 self.flops += 10 * w.d * w.hq * cpa.visible_pairs(qmap, nq, kmap, nk, w.causal)
+            if fused:
+                # the block's whole chunk list in one call (one launch per 32 chunks)
+                self.calls.append((cpa.partial_attn_bwd_chunks,
+                                   dict(q=qb, d_o=d_o, aux=aux, q_pos=qmap, chunks=clist, dq=dq, causal=w.causal)))
+            else:
+                for k, v, kmap, dk, dv in clist:
+                    self.calls.append((cpa.partial_attn_bwd, dict(q=qb, k=k, v=v, d_o=d_o, aux=aux, q_pos=qmap,
+                                                                  kv_pos=kmap, dq=dq, dk=dk, dv=dv, causal=w.causal)))
 
     def run(self, timers=None):
         stream = torch.cuda.current_stream()
@@ -373,13 +381,15 @@ class BwdStep:
         if timers is not None:
             a = torch.cuda.Event(enable_timing=True)
             a.record(stream)
-        for kw in self.calls:
-            self.cpa.partial_attn_bwd(**kw)
+        launches = 0
+        for fn, kw in self.calls:
+            fn(**kw)
+            launches += (len(kw["chunks"]) + 31) // 32 if "chunks" in kw else 1
         if timers is not None:
             b = torch.cuda.Event(enable_timing=True)
             b.record(stream)
             timers.append((a, b))
-        return len(self.preps) + len(self.calls)
+        return len(self.preps) + launches
 
 
 class UlyssesBwdStep:
@@ -814,7 +824,7 @@ def run_gpu(args):
                     "path": ("dO seq->head, per head-rank prep + full-sequence cp_partial_attn_bwd, "
                              "dQ and dK|dV head->seq (fp32); gradients zeroed in the step")
                     if args.config == 4 else
-                    ("prep per query block + one cp_partial_attn_bwd per (block, chunk); "
+                    ("prep per query block + one cp_partial_attn_bwd_chunks per block over its chunk list; "
                      "dK/dV accumulated into the chunk owners' shards; gradients zeroed in the step")}
         if rtimes:
             r_ms = sum(s_.elapsed_time(e_) for s_, e_ in rtimes) / args.steps

@@ -17,6 +17,7 @@ from .api import (  # noqa: F401
     merge_partials,
     attn_bwd_prep,
     partial_attn_bwd,
+    partial_attn_bwd_chunks,
     bwd_aux_floats,
     ulysses_reshard,
     library_path,
@@ -37,6 +38,7 @@ __all__ = [
     "merge_partials",
     "attn_bwd_prep",
     "partial_attn_bwd",
+    "partial_attn_bwd_chunks",
     "bwd_aux_floats",
     "ulysses_reshard",
     "library_path",

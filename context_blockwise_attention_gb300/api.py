@@ -63,6 +63,11 @@ class _AttnBwdDesc(ctypes.Structure):
     ]
 
 
+class _KvBwdChunk(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("dk", ctypes.c_void_p),
+                ("dv", ctypes.c_void_p), ("skv", ctypes.c_int64), ("kv_pos", _PosMap)]
+
+
 class _KvChunk(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("skv", ctypes.c_int64),
                 ("kv_pos", _PosMap)]
@@ -109,6 +114,8 @@ def load_library():
     lib.cp_attn_bwd_prep.argtypes = [vp, i32, vp, i32, vp, i64, i32, i32, vp, vp]
     lib.cp_partial_attn_bwd.restype = i32
     lib.cp_partial_attn_bwd.argtypes = [ctypes.POINTER(_AttnBwdDesc), vp]
+    lib.cp_partial_attn_bwd_chunks.restype = i32
+    lib.cp_partial_attn_bwd_chunks.argtypes = [ctypes.POINTER(_AttnBwdDesc), i32, ctypes.POINTER(_KvBwdChunk), vp]
     lib.cp_merge_partials.restype = i32
     lib.cp_merge_partials.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), i64, i32, i32,
                                       vp, i32, vp, vp]
@@ -365,6 +372,57 @@ def partial_attn_bwd(q, k, v, d_o, aux, q_pos: PosMap, kv_pos: PosMap, dq, dk, d
     desc.flags = int(flags)
     _check(lib.cp_partial_attn_bwd(ctypes.byref(desc), _stream(stream)))
     return dq, dk, dv
+
+
+def partial_attn_bwd_chunks(q, d_o, aux, q_pos: PosMap, chunks, dq, causal=True, scale=0.0, status=None,
+                            wait_timeout_ms=0, flags=0, stream=None):
+    """The backward of query shard ``q`` against a list of chunks ``(k, v, kv_pos, dk, dv)`` in one
+    call: the same as ``partial_attn_bwd`` per chunk (accumulating into ``dq`` and each chunk's
+    ``dk``, ``dv``), with one launch per 32 chunks."""
+    lib = load_library()
+    for t, n in ((q, "q"), (d_o, "d_o"), (aux, "aux"), (dq, "dq")):
+        _need_cuda(t, n)
+    if q.dim() != 3 or d_o.shape != q.shape or dq.shape != q.shape or dq.dtype != torch.float32:
+        raise CpError(CP_ERR_INVALID_ARG, "q, d_o [Sq, Hq, D]; dq fp32 of the same shape")
+    sq, hq, d = q.shape
+    if aux.dtype != torch.float32 or aux.numel() < bwd_aux_floats(sq, hq):
+        raise CpError(CP_ERR_INVALID_ARG, "aux must be fp32 with bwd_aux_floats(sq, hq) elements")
+    if not 1 <= len(chunks) <= CP_MAX_CHUNKS:
+        raise CpError(CP_ERR_INVALID_ARG, f"1..{CP_MAX_CHUNKS} chunks expected")
+    arr = (_KvBwdChunk * len(chunks))()
+    hkv = None
+    for i, (k, v, kv_pos, dk, dv) in enumerate(chunks):
+        for t, n in ((k, "k"), (v, "v"), (dk, "dk"), (dv, "dv")):
+            _need_cuda(t, n)
+        if k.dim() != 3 or v.shape != k.shape or k.shape[2] != d or k.dtype != q.dtype or v.dtype != q.dtype:
+            raise CpError(CP_ERR_INVALID_ARG, f"chunk {i}: k and v must be [Skv, Hkv, D] of q's dtype")
+        if dk.shape != k.shape or dv.shape != k.shape or dk.dtype != torch.float32 or dv.dtype != torch.float32:
+            raise CpError(CP_ERR_INVALID_ARG, f"chunk {i}: dk and dv must be fp32 shaped like k")
+        if hkv is None:
+            hkv = k.shape[1]
+        elif k.shape[1] != hkv:
+            raise CpError(CP_ERR_INVALID_ARG, "every chunk must have the same KV head count")
+        arr[i].k, arr[i].v, arr[i].dk, arr[i].dv = k.data_ptr(), v.data_ptr(), dk.data_ptr(), dv.data_ptr()
+        arr[i].skv = k.shape[0]
+        arr[i].kv_pos = _PosMap(kv_pos.base, kv_pos.stride)
+    desc = _AttnBwdDesc()
+    desc.q, desc.d_o = q.data_ptr(), d_o.data_ptr()
+    desc.in_dtype = _dtype_code(q.dtype)
+    desc.aux = aux.data_ptr()
+    desc.dq = dq.data_ptr()
+    desc.sq, desc.hq, desc.hkv, desc.d = sq, hq, hkv, d
+    desc.causal = 1 if causal else 0
+    desc.scale = float(scale)
+    desc.q_pos = _PosMap(q_pos.base, q_pos.stride)
+    if status is not None:
+        _need_cuda(status, "status")
+        if status.dtype != torch.int32:
+            raise CpError(CP_ERR_INVALID_ARG, "status must be int32")
+        desc.status = status.data_ptr()
+    desc.wait_timeout_ms = int(wait_timeout_ms)
+    desc.flags = int(flags)
+    _check(lib.cp_partial_attn_bwd_chunks(ctypes.byref(desc), len(chunks), arr, _stream(stream)))
+    return dq
 
 
 def merge_partials(o_parts, lse_parts, out_dtype=torch.bfloat16, o=None, lse=None, stream=None):

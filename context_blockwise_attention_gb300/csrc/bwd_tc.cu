@@ -48,6 +48,7 @@ namespace {
 constexpr int kRows = 128;     // query rows per tile
 constexpr int kKeys = 128;     // keys per KV tile
 constexpr int kThreads = 384;  // 12 warps
+constexpr int kBwdMaxChunksPerLaunch = 32;  // chunk table size limit (kernel parameter space)
 
 enum BwdSite : int {
   kSKvFull = 1,
@@ -70,14 +71,31 @@ enum BwdSite : int {
 struct BwdParams {
   int32_t* status;
   const float* aux;  // [2][hq][sq_pad]: -LSE*log2(e), -D
-  int64_t sq, skv, sq_pad;
+  int64_t sq, sq_pad;
   int32_t hq, hkv, group, causal;
-  int32_t n_qt, n_kt;  // query tiles, KV tiles
-  int64_t n_units;     // n_kt * hq
+  int32_t n_qt;        // query tiles
+  int32_t max_kt;      // KV tiles of the longest chunk
+  int64_t n_units;     // max_kt * n_chunks * hq
   float scale, sl2;    // scale, scale * log2(e)
-  int64_t q_base, q_stride, k_base, k_stride;
+  int64_t q_base, q_stride;
   int64_t timeout_ns;
   int32_t test_stall;  // test only: block 0's MMA warp first waits on a barrier nothing completes
+};
+
+// The KV chunks of one launch: TMA maps of K, V ([skv, hkv*d] bf16) and of their gradients dK,
+// dV ([skv, hkv*d] fp32, reduction targets), token counts and affine global positions.  Chunks
+// are independent here (each adds its own share); one launch just saves launches and lets the
+// units of all chunks share one schedule.
+template <int MAXC>
+struct BwdChunks {
+  CUtensorMap k[MAXC];
+  CUtensorMap v[MAXC];
+  CUtensorMap dk[MAXC];
+  CUtensorMap dv[MAXC];
+  int64_t skv[MAXC];
+  int64_t base[MAXC];
+  int64_t stride[MAXC];
+  int32_t n;
 };
 
 template <int D>
@@ -128,19 +146,29 @@ struct Bars {
 };
 
 struct BUnit {
+  int c;      // chunk
   int jt, h, g;
-  int t0;   // first query tile that sees the KV tile
-  int nit;  // query tiles to visit
+  int t0;     // first query tile that sees the KV tile
+  int nit;    // query tiles to visit (0: nothing to do)
 };
 
-__device__ __forceinline__ BUnit decode_bunit(const BwdParams& p, int64_t u) {
+// Units are (KV tile index, chunk, head) with the KV tile outermost: earliest keys first across
+// every chunk (they see the most query tiles), so the snake deal stays longest-first.  Tiles past
+// a shorter chunk's end are empty units.
+template <int MAXC>
+__device__ __forceinline__ BUnit decode_bunit(const BwdParams& p, const BwdChunks<MAXC>& ch, int64_t u) {
   BUnit w;
-  w.jt = static_cast<int>(u / p.hq);
-  w.h = static_cast<int>(u % p.hq);
+  const int64_t per_tile = static_cast<int64_t>(ch.n) * p.hq;
+  w.jt = static_cast<int>(u / per_tile);
+  const int64_t rem = u - static_cast<int64_t>(w.jt) * per_tile;
+  w.c = static_cast<int>(rem / p.hq);
+  w.h = static_cast<int>(rem - static_cast<int64_t>(w.c) * p.hq);
   w.g = w.h / p.group;
   w.t0 = 0;
-  if (p.causal) {
-    const int64_t kp0 = p.k_base + p.k_stride * static_cast<int64_t>(w.jt) * kKeys;
+  if (static_cast<int64_t>(w.jt) * kKeys >= ch.skv[w.c]) {
+    w.t0 = p.n_qt;
+  } else if (p.causal) {
+    const int64_t kp0 = ch.base[w.c] + ch.stride[w.c] * static_cast<int64_t>(w.jt) * kKeys;
     int64_t rmin = 0;  // first query row whose position reaches the tile's first key
     if (kp0 > p.q_base) rmin = (kp0 - p.q_base + p.q_stride - 1) / p.q_stride;
     w.t0 = rmin >= p.sq ? p.n_qt : static_cast<int>(rmin / kRows);
@@ -176,12 +204,11 @@ __device__ __forceinline__ uint32_t reduce_box(uint32_t stage0, int lane, uint32
   return nred + 1;
 }
 
-template <int D>
+template <int D, int MAXC>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_tc_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap tm_q,
-                       const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dq,
-                       const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv) {
+                       const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dq,
+                       const __grid_constant__ BwdChunks<MAXC> ch) {
   using L = BLayout<D>;
   using namespace sync;
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -264,8 +291,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (leader) {
         ptx::tma_prefetch_desc(&tm_q);
         ptx::tma_prefetch_desc(&tm_do);
-        ptx::tma_prefetch_desc(&tm_k);
-        ptx::tma_prefetch_desc(&tm_v);
+        for (int c = 0; c < ch.n; ++c) {
+          ptx::tma_prefetch_desc(&ch.k[c]);
+          ptx::tma_prefetch_desc(&ch.v[c]);
+        }
       }
       int64_t gi = 0, ku = 0;  // query tiles and units with work issued so far
       int64_t ql = 0, dl = 0;  // Q and dO loads issued
@@ -273,14 +302,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t k = 0; ok; ++k) {
         const int64_t u = unit_of(k, cta, grid);
         if (u >= p.n_units) break;
-        const BUnit w = decode_bunit(p, u);
+        const BUnit w = decode_bunit(p, ch, u);
         if (w.nit <= 0) continue;
         if (ku > 0 && !(ok = wait_warp(b.kv_empty, static_cast<uint32_t>((ku - 1) & 1), ctl, kSKvEmpty))) break;
         if (leader) {
           ptx::mbar_arrive_expect_tx(b.kv_full, 2 * L::kTileBytes);
           for (int cc = 0; cc < L::kChunks; ++cc) {
-            ptx::tma_load_2d(sK + cc * L::kChunkBytes, &tm_k, w.g * D + cc * 64, w.jt * kKeys, b.kv_full);
-            ptx::tma_load_2d(sV + cc * L::kChunkBytes, &tm_v, w.g * D + cc * 64, w.jt * kKeys, b.kv_full);
+            ptx::tma_load_2d(sK + cc * L::kChunkBytes, &ch.k[w.c], w.g * D + cc * 64, w.jt * kKeys, b.kv_full);
+            ptx::tma_load_2d(sV + cc * L::kChunkBytes, &ch.v[w.c], w.g * D + cc * 64, w.jt * kKeys, b.kv_full);
           }
         }
         __syncwarp();
@@ -391,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t k = 0; ok; ++k) {
         const int64_t u = unit_of(k, cta, grid);
         if (u >= p.n_units) break;
-        const BUnit w = decode_bunit(p, u);
+        const BUnit w = decode_bunit(p, ch, u);
         if (w.nit <= 0) continue;
         if (!(ok = wait_warp(b.kv_full, static_cast<uint32_t>(ku & 1), ctl, kSKvFull))) break;
         if (!(ok = issue_s(gi))) break;
@@ -466,21 +495,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t k = 0; ok; ++k) {
       const int64_t u = unit_of(k, cta, grid);
       if (u >= p.n_units) break;
-      const BUnit w = decode_bunit(p, u);
+      const BUnit w = decode_bunit(p, ch, u);
       if (w.nit <= 0) continue;
       const int64_t key = static_cast<int64_t>(w.jt) * kKeys + r;
-      const int64_t kpos = p.k_base + p.k_stride * key;
+      const int64_t kpos = ch.base[w.c] + ch.stride[w.c] * key;
+      const int64_t skv = ch.skv[w.c];
       int64_t rmin_k = 0;  // first query row that sees this key
       if (p.causal && kpos > p.q_base) rmin_k = (kpos - p.q_base + p.q_stride - 1) / p.q_stride;
       // rows past the chunk's end (zero-filled K, V) get P = 0 too: against a very negative LSE
       // their exponent could overflow, and 0 * inf would reach dQ
-      if (key >= p.skv) rmin_k = INT64_MAX / 2;
+      if (key >= skv) rmin_k = INT64_MAX / 2;
       for (int it = 0; it < w.nit; ++it, ++gi) {
         const int t = w.t0 + it;
         const int st = static_cast<int>(gi % L::kQStages);
         const uint32_t cur = static_cast<uint32_t>(gi & 1);
         int cmin = 0;  // query columns below cmin do not see this key
-        if (p.causal || key >= p.skv) {
+        if (p.causal || key >= skv) {
           const int64_t c = rmin_k - static_cast<int64_t>(t) * kRows;
           cmin = c <= 0 ? 0 : (c >= kRows ? kRows : static_cast<int>(c));
         }
@@ -587,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t k = 0; ok; ++k) {
       const int64_t u = unit_of(k, cta, grid);
       if (u >= p.n_units) break;
-      const BUnit w = decode_bunit(p, u);
+      const BUnit w = decode_bunit(p, ch, u);
       if (w.nit <= 0) continue;
       for (int it = 0; it < w.nit; ++it, ++gi) {
         const int t = w.t0 + it;
@@ -619,14 +649,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t v[32];
         ptx::tmem_ld32(tmem + L::kColDK + lane_bits + c * 32, v);
         ptx::tmem_wait_ld();
-        nred = reduce_box<L::kStageBufs>(stage0, lane, nred, v, p.scale, &tm_dk, w.g * D + c * 32, w.jt * kKeys + wq * 32, p.skv);
+        nred = reduce_box<L::kStageBufs>(stage0, lane, nred, v, p.scale, &ch.dk[w.c], w.g * D + c * 32, w.jt * kKeys + wq * 32,
+                                         ch.skv[w.c]);
       }
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
         ptx::tmem_ld32(tmem + L::kColDV + lane_bits + c * 32, v);
         ptx::tmem_wait_ld();
-        nred = reduce_box<L::kStageBufs>(stage0, lane, nred, v, 1.0f, &tm_dv, w.g * D + c * 32, w.jt * kKeys + wq * 32, p.skv);
+        nred = reduce_box<L::kStageBufs>(stage0, lane, nred, v, 1.0f, &ch.dv[w.c], w.g * D + c * 32, w.jt * kKeys + wq * 32,
+                                         ch.skv[w.c]);
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -645,53 +677,91 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
-cp_status launch_bwd_d(const BwdParams& p, const cp_attn_bwd_desc& d, int64_t grid, cudaStream_t s) {
-  CUtensorMap mq, mdo, mk, mv, mdq, mdk, mdv;
-  const int64_t qe = int64_t(d.hq) * D, ke = int64_t(d.hkv) * D;
+template <int D, int MAXC>
+cp_status launch_bwd_dc(const BwdParams& p0, const cp_attn_bwd_desc& d, const cp_kv_bwd_chunk* chunks, int n,
+                        int num_sms, cudaStream_t s) {
+  BwdChunks<MAXC> ch;
+  memset(&ch, 0, sizeof(ch));
+  ch.n = n;
+  BwdParams p = p0;
+  const int64_t ke = int64_t(d.hkv) * D;
+  int64_t max_kt = 0;
+  for (int c = 0; c < n; ++c) {
+    const cp_kv_bwd_chunk& k = chunks[c];
+    if (!encode_map_2d(&ch.k[c], k.k, k.skv, ke, false, 128) || !encode_map_2d(&ch.v[c], k.v, k.skv, ke, false, 128) ||
+        !encode_map_2d(&ch.dk[c], k.dk, k.skv, ke, true, 32) || !encode_map_2d(&ch.dv[c], k.dv, k.skv, ke, true, 32)) {
+      set_error("cuTensorMapEncodeTiled failed for chunk %d (or the driver entry point is unavailable)", c);
+      return CP_ERR_CUDA;
+    }
+    ch.skv[c] = k.skv;
+    ch.base[c] = k.kv_pos.base;
+    ch.stride[c] = k.kv_pos.stride;
+    const int64_t kt = (k.skv + kKeys - 1) / kKeys;
+    if (kt > max_kt) max_kt = kt;
+  }
+  p.max_kt = static_cast<int32_t>(max_kt);
+  p.n_units = max_kt * n * d.hq;
+  CUtensorMap mq, mdo, mdq;
+  const int64_t qe = int64_t(d.hq) * D;
   if (!encode_map_2d(&mq, d.q, d.sq, qe, false, 128) || !encode_map_2d(&mdo, d.d_o, d.sq, qe, false, 128) ||
-      !encode_map_2d(&mk, d.k, d.skv, ke, false, 128) || !encode_map_2d(&mv, d.v, d.skv, ke, false, 128) ||
-      !encode_map_2d(&mdq, d.dq, d.sq, qe, true, 32) || !encode_map_2d(&mdk, d.dk, d.skv, ke, true, 32) ||
-      !encode_map_2d(&mdv, d.dv, d.skv, ke, true, 32)) {
+      !encode_map_2d(&mdq, d.dq, d.sq, qe, true, 32)) {
     set_error("cuTensorMapEncodeTiled failed (or the driver entry point is unavailable)");
     return CP_ERR_CUDA;
   }
+  const int64_t grid = p.n_units < num_sms ? p.n_units : num_sms;
   constexpr int smem = BLayout<D>::kSmemLaunch;
-  cudaError_t e = cudaFuncSetAttribute(attn_bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(attn_bwd_tc_kernel<D, MAXC>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attn_bwd_tc_kernel)");
-  attn_bwd_tc_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p, mq, mdo, mk, mv, mdq, mdk, mdv);
+  attn_bwd_tc_kernel<D, MAXC><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p, mq, mdo, mdq, ch);
   e = cudaGetLastError();
   return e == cudaSuccess ? CP_OK : cuda_fail(e, "attn_bwd_tc_kernel launch");
 }
 
+template <int D>
+cp_status launch_bwd_d(const BwdParams& p, const cp_attn_bwd_desc& d, const cp_kv_bwd_chunk* chunks, int n,
+                       int num_sms, cudaStream_t s) {
+  // the chunk table travels in the kernel parameters: size it to the call; longer lists go in
+  // batches (the chunks are independent)
+  for (int at = 0; at < n;) {
+    const int m = (n - at) < kBwdMaxChunksPerLaunch ? (n - at) : kBwdMaxChunksPerLaunch;
+    cp_status st;
+    if (m == 1)
+      st = launch_bwd_dc<D, 1>(p, d, chunks + at, m, num_sms, s);
+    else if (m <= 8)
+      st = launch_bwd_dc<D, 8>(p, d, chunks + at, m, num_sms, s);
+    else
+      st = launch_bwd_dc<D, kBwdMaxChunksPerLaunch>(p, d, chunks + at, m, num_sms, s);
+    if (st != CP_OK) return st;
+    at += m;
+  }
+  return CP_OK;
+}
+
 }  // namespace
 
-cp_status launch_partial_attn_bwd_tc(const cp_attn_bwd_desc& d, float scale, int64_t timeout_ns, int num_sms,
-                                     cudaStream_t s) {
+cp_status launch_partial_attn_bwd_tc(const cp_attn_bwd_desc& d, const cp_kv_bwd_chunk* chunks, int n, float scale,
+                                     int64_t timeout_ns, int num_sms, cudaStream_t s) {
   BwdParams p;
   p.status = d.status;
   p.aux = d.aux;
   p.sq = d.sq;
-  p.skv = d.skv;
   p.sq_pad = (d.sq + 127) / 128 * 128;
   p.hq = d.hq;
   p.hkv = d.hkv;
   p.group = d.hq / d.hkv;
   p.causal = d.causal;
   p.n_qt = static_cast<int32_t>((d.sq + kRows - 1) / kRows);
-  p.n_kt = static_cast<int32_t>((d.skv + kKeys - 1) / kKeys);
-  p.n_units = static_cast<int64_t>(p.n_kt) * d.hq;
+  p.max_kt = 0;
+  p.n_units = 0;
   p.scale = scale;
   p.sl2 = scale * 1.4426950408889634f;
   p.q_base = d.q_pos.base;
   p.q_stride = d.q_pos.stride;
-  p.k_base = d.kv_pos.base;
-  p.k_stride = d.kv_pos.stride;
   p.timeout_ns = timeout_ns;
   p.test_stall = (d.flags & CP_FLAG_TEST_STALL) ? 1 : 0;
-  const int64_t grid = p.n_units < num_sms ? p.n_units : num_sms;
-  if (d.d == 64) return launch_bwd_d<64>(p, d, grid, s);
-  return launch_bwd_d<128>(p, d, grid, s);
+  if (d.d == 64) return launch_bwd_d<64>(p, d, chunks, n, num_sms, s);
+  return launch_bwd_d<128>(p, d, chunks, n, num_sms, s);
 }
 
 }  // namespace cpattn

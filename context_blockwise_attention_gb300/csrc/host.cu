@@ -283,44 +283,106 @@ CP_API cp_status cp_attn_bwd_prep(const void* o, int32_t o_dtype, const void* d_
   return launch_bwd_prep(o, o_dtype == CP_BF16, d_o, do_dtype == CP_BF16, lse, sq, hq, d, aux, sms, stream);
 }
 
-CP_API cp_status cp_partial_attn_bwd(const cp_attn_bwd_desc* desc, cudaStream_t stream) {
-  clear_error();
-  if (desc == nullptr) CP_INVALID("cp_partial_attn_bwd: desc is NULL");
-  const cp_attn_bwd_desc& d = *desc;
+// Checks every backward descriptor field except k, v, dk, dv, skv and kv_pos.
+static cp_status validate_bwd_desc(const cp_attn_bwd_desc& d) {
   if (d.in_dtype != CP_F32 && d.in_dtype != CP_BF16)
     CP_INVALID("partial attention backward: in_dtype %d is not CP_F32 or CP_BF16", d.in_dtype);
-  if (d.sq < 0 || d.skv < 0) CP_INVALID("partial attention backward: negative token count");
-  if (d.sq > (int64_t(1) << 31) - 256 || d.skv > (int64_t(1) << 31) - 256)
-    CP_INVALID("partial attention backward: token counts must stay below 2^31");
+  if (d.sq < 0) CP_INVALID("partial attention backward: negative token count");
+  if (d.sq > (int64_t(1) << 31) - 256) CP_INVALID("partial attention backward: token counts must stay below 2^31");
   if (d.hq <= 0 || d.hkv <= 0) CP_INVALID("partial attention backward: head counts must be positive");
   if (d.hq % d.hkv != 0) CP_INVALID("partial attention backward: hq %d is not a multiple of hkv %d", d.hq, d.hkv);
   if (d.d != 64 && d.d != 128) CP_INVALID("partial attention backward: head_dim %d not in {64, 128}", d.d);
   if (d.causal != 0 && d.causal != 1) CP_INVALID("partial attention backward: causal must be 0 or 1");
-  if (d.q_pos.stride < 1 || d.kv_pos.stride < 1) CP_INVALID("partial attention backward: position strides must be >= 1");
-  if (d.q_pos.base < 0 || d.kv_pos.base < 0) CP_INVALID("partial attention backward: positions must be >= 0");
-  if (double(d.q_pos.base) + double(d.q_pos.stride) * double(d.sq) > 2.0e9 ||
-      double(d.kv_pos.base) + double(d.kv_pos.stride) * double(d.skv) > 2.0e9)
+  if (d.q_pos.stride < 1) CP_INVALID("partial attention backward: position strides must be >= 1");
+  if (d.q_pos.base < 0) CP_INVALID("partial attention backward: positions must be >= 0");
+  if (double(d.q_pos.base) + double(d.q_pos.stride) * double(d.sq) > 2.0e9)
     CP_INVALID("partial attention backward: global positions exceed 2e9");
   if (!(d.scale >= 0.0f) || isinf(d.scale)) CP_INVALID("partial attention backward: scale must be finite and >= 0");
   if (d.flags & ~CP_FLAG_TEST_STALL) CP_INVALID("partial attention backward: unknown flag bits 0x%x", d.flags);
   if ((d.flags & CP_FLAG_TEST_STALL) && d.in_dtype != CP_BF16)
     CP_INVALID("partial attention backward: CP_FLAG_TEST_STALL applies to the bf16 (tensor-core) path only");
   if (d.wait_timeout_ms < 0) CP_INVALID("partial attention backward: wait_timeout_ms must be >= 0");
-  if (d.sq == 0 || d.skv == 0) return CP_OK;  // nothing to add
-  if (d.q == nullptr || d.k == nullptr || d.v == nullptr || d.d_o == nullptr || d.aux == nullptr ||
-      d.dq == nullptr || d.dk == nullptr || d.dv == nullptr)
-    CP_INVALID("partial attention backward: q, k, v, d_o, aux, dq, dk and dv must not be NULL");
-  if (!aligned16(d.q) || !aligned16(d.k) || !aligned16(d.v) || !aligned16(d.d_o) || !aligned16(d.aux) ||
-      !aligned16(d.dq) || !aligned16(d.dk) || !aligned16(d.dv))
-    CP_INVALID("partial attention backward: every buffer must be 16-byte aligned");
+  if (d.sq > 0) {
+    if (d.q == nullptr || d.d_o == nullptr || d.aux == nullptr || d.dq == nullptr)
+      CP_INVALID("partial attention backward: q, d_o, aux and dq must not be NULL");
+    if (!aligned16(d.q) || !aligned16(d.d_o) || !aligned16(d.aux) || !aligned16(d.dq))
+      CP_INVALID("partial attention backward: every buffer must be 16-byte aligned");
+  }
+  return CP_OK;
+}
+
+static cp_status validate_bwd_chunk(const cp_attn_bwd_desc& d, const cp_kv_bwd_chunk& c, int idx) {
+  if (c.skv < 0) CP_INVALID("partial attention backward: chunk %d has a negative token count", idx);
+  if (c.skv > (int64_t(1) << 31) - 256) CP_INVALID("partial attention backward: chunk %d token count must stay below 2^31", idx);
+  if (c.kv_pos.stride < 1) CP_INVALID("partial attention backward: chunk %d position stride must be >= 1", idx);
+  if (c.kv_pos.base < 0) CP_INVALID("partial attention backward: chunk %d positions must be >= 0", idx);
+  if (double(c.kv_pos.base) + double(c.kv_pos.stride) * double(c.skv) > 2.0e9)
+    CP_INVALID("partial attention backward: chunk %d global positions exceed 2e9", idx);
+  if (c.skv > 0 && d.sq > 0) {
+    if (c.k == nullptr || c.v == nullptr || c.dk == nullptr || c.dv == nullptr)
+      CP_INVALID("partial attention backward: chunk %d k, v, dk and dv must not be NULL", idx);
+    if (!aligned16(c.k) || !aligned16(c.v) || !aligned16(c.dk) || !aligned16(c.dv))
+      CP_INVALID("partial attention backward: chunk %d buffers must be 16-byte aligned", idx);
+  }
+  return CP_OK;
+}
+
+static cp_status run_partial_bwd(const cp_attn_bwd_desc& d, const cp_kv_bwd_chunk* chunks, int n,
+                                 cudaStream_t stream) {
+  if (d.sq == 0) return CP_OK;  // nothing to add
+  cp_kv_bwd_chunk live[CP_MAX_CHUNKS];
+  int m = 0;
+  for (int i = 0; i < n; ++i)
+    if (chunks[i].skv > 0) live[m++] = chunks[i];
+  if (m == 0) return CP_OK;
   int dev = 0, sms = 0;
   cp_status st = require_sm103(&dev, &sms);
   if (st != CP_OK) return st;
   const float scale = d.scale > 0.0f ? d.scale : 1.0f / sqrtf(static_cast<float>(d.d));
   const int64_t timeout_ns =
       static_cast<int64_t>(d.wait_timeout_ms > 0 ? d.wait_timeout_ms : 2000) * 1000000LL;
-  if (d.in_dtype == CP_F32) return launch_partial_attn_bwd_simt(d, scale, stream);
-  return launch_partial_attn_bwd_tc(d, scale, timeout_ns, sms, stream);
+  if (d.in_dtype == CP_BF16) return launch_partial_attn_bwd_tc(d, live, m, scale, timeout_ns, sms, stream);
+  for (int i = 0; i < m; ++i) {  // fp32: one exclusive-owner pass per chunk
+    cp_attn_bwd_desc one = d;
+    one.k = live[i].k;
+    one.v = live[i].v;
+    one.dk = live[i].dk;
+    one.dv = live[i].dv;
+    one.skv = live[i].skv;
+    one.kv_pos = live[i].kv_pos;
+    if ((st = launch_partial_attn_bwd_simt(one, scale, stream)) != CP_OK) return st;
+  }
+  return CP_OK;
+}
+
+CP_API cp_status cp_partial_attn_bwd(const cp_attn_bwd_desc* desc, cudaStream_t stream) {
+  clear_error();
+  if (desc == nullptr) CP_INVALID("cp_partial_attn_bwd: desc is NULL");
+  cp_status st = validate_bwd_desc(*desc);
+  if (st != CP_OK) return st;
+  cp_kv_bwd_chunk c;
+  c.k = desc->k;
+  c.v = desc->v;
+  c.dk = desc->dk;
+  c.dv = desc->dv;
+  c.skv = desc->skv;
+  c.kv_pos = desc->kv_pos;
+  if ((st = validate_bwd_chunk(*desc, c, 0)) != CP_OK) return st;
+  return run_partial_bwd(*desc, &c, 1, stream);
+}
+
+CP_API cp_status cp_partial_attn_bwd_chunks(const cp_attn_bwd_desc* desc, int32_t n_chunks,
+                                            const cp_kv_bwd_chunk* chunks, cudaStream_t stream) {
+  clear_error();
+  if (desc == nullptr) CP_INVALID("cp_partial_attn_bwd_chunks: desc is NULL");
+  if (n_chunks < 1 || n_chunks > CP_MAX_CHUNKS)
+    CP_INVALID("cp_partial_attn_bwd_chunks: n_chunks=%d not in [1, %d]", n_chunks, CP_MAX_CHUNKS);
+  if (chunks == nullptr) CP_INVALID("cp_partial_attn_bwd_chunks: chunks is NULL");
+  cp_status st = validate_bwd_desc(*desc);
+  if (st != CP_OK) return st;
+  for (int i = 0; i < n_chunks; ++i)
+    if ((st = validate_bwd_chunk(*desc, chunks[i], i)) != CP_OK) return st;
+  return run_partial_bwd(*desc, chunks, n_chunks, stream);
 }
 
 CP_API cp_status cp_merge_partials(int32_t n, const float* const* o_parts,

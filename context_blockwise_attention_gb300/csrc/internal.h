@@ -43,9 +43,11 @@ cp_status launch_fill_empty(const cp_attn_desc& d, cudaStream_t s);
 // Backward pass (arguments validated by the entry points).
 cp_status launch_bwd_prep(const void* o, bool o_bf16, const void* d_o, bool do_bf16, const float* lse,
                           int64_t sq, int32_t hq, int32_t d, float* aux, int num_sms, cudaStream_t s);
+// One chunk (desc's k, v, dk, dv, skv, kv_pos), fp32 inputs.
 cp_status launch_partial_attn_bwd_simt(const cp_attn_bwd_desc& d, float scale, cudaStream_t s);
-cp_status launch_partial_attn_bwd_tc(const cp_attn_bwd_desc& d, float scale, int64_t timeout_ns, int num_sms,
-                                     cudaStream_t s);
+// chunks[0..n), each with skv > 0; bf16 inputs.
+cp_status launch_partial_attn_bwd_tc(const cp_attn_bwd_desc& d, const cp_kv_bwd_chunk* chunks, int n, float scale,
+                                     int64_t timeout_ns, int num_sms, cudaStream_t s);
 
 struct MergeArgs {
   int32_t n;

@@ -316,6 +316,27 @@ typedef struct {
 
 cp_status cp_partial_attn_bwd(const cp_attn_bwd_desc* desc, cudaStream_t stream);
 
+/* One KV chunk for cp_partial_attn_bwd_chunks: device K, V [skv, hkv, d] (in_dtype), the chunk's
+ * gradient buffers dK, dV [skv, hkv, d] (fp32, accumulated), and its global positions. */
+typedef struct {
+  const void* k;
+  const void* v;
+  float* dk;
+  float* dv;
+  int64_t skv;
+  cp_posmap kv_pos;
+} cp_kv_bwd_chunk;
+
+/*
+ * The backward of one query shard against a list of KV chunks in one call (f1's counterpart):
+ * the same as one cp_partial_attn_bwd per chunk (desc's k, v, dk, dv, skv and kv_pos are
+ * ignored), with the chunks' work dealt out in one persistent launch per 32 chunks.  The order of
+ * the chunks does not matter (each adds its own share).  n_chunks in [1, CP_MAX_CHUNKS].
+ * Errors: as cp_partial_attn_bwd, per chunk.
+ */
+cp_status cp_partial_attn_bwd_chunks(const cp_attn_bwd_desc* desc, int32_t n_chunks,
+                                     const cp_kv_bwd_chunk* chunks, cudaStream_t stream);
+
 /* Message for the calling thread's last non-OK status ("" if none).  Valid until the next call. */
 const char* cp_last_error(void);
 

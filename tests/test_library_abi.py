@@ -259,3 +259,24 @@ def test_bwd_test_stall_needs_bf16():
     d = _bwd_desc(flags=api.CP_FLAG_TEST_STALL, in_dtype=api.CP_F32)
     assert lib.cp_partial_attn_bwd(ctypes.byref(d), None) == api.CP_ERR_INVALID_ARG
 
+
+def test_bwd_chunks_rejects():
+    lib = cpa.load_library()
+    assert ctypes.sizeof(api._KvBwdChunk) == 56
+    d = _bwd_desc()
+    arr = (api._KvBwdChunk * 2)()
+    for i in range(2):
+        arr[i].k = arr[i].v = 0x1000
+        arr[i].dk = arr[i].dv = 0x2000
+        arr[i].skv = 128
+        arr[i].kv_pos = api._PosMap(0, 1)
+    assert lib.cp_partial_attn_bwd_chunks(ctypes.byref(d), 0, arr, None) == api.CP_ERR_INVALID_ARG
+    assert lib.cp_partial_attn_bwd_chunks(ctypes.byref(d), 65, arr, None) == api.CP_ERR_INVALID_ARG
+    assert lib.cp_partial_attn_bwd_chunks(ctypes.byref(d), 2, None, None) == api.CP_ERR_INVALID_ARG
+    assert lib.cp_partial_attn_bwd_chunks(None, 2, arr, None) == api.CP_ERR_INVALID_ARG
+    arr[1].dv = 0
+    assert lib.cp_partial_attn_bwd_chunks(ctypes.byref(d), 2, arr, None) == api.CP_ERR_INVALID_ARG
+    arr[1].dv = 0x2000
+    arr[1].kv_pos = api._PosMap(0, 0)
+    assert lib.cp_partial_attn_bwd_chunks(ctypes.byref(d), 2, arr, None) == api.CP_ERR_INVALID_ARG
+
