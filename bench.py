@@ -27,6 +27,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -329,7 +330,7 @@ class Step:
 
 
 class BwdStep:
-    """Backward of a step's attention (SURVEY f4): per query block the prep kernel (from the
+    """Backward of a step's attention: per query block the prep kernel (from the
     block's final O and LSE, produced by running `fwd` once), then the partial backward of every
     (query block, visible chunk) pair -- one chunk-list call per block (`fused`, default) or one
     call per pair in arrival order; dQ accumulates per block, dK and dV into the chunk owner's
@@ -483,7 +484,9 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        # the raw samples go to CPATTN_CLOCKS_DIR (default: the system temporary directory)
+        out_dir = os.environ.get("CPATTN_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"clocks_gpu{gpu_index}.csv")
 
     def start(self):
         try:
@@ -730,7 +733,7 @@ def run_gpu(args):
                                             "attn_tc.cu"), f"cfg{args.config}")
     if w.dtype == "f32":
         # fp32 inputs run on CUDA cores (FFMA): the peak is SMs x 128 FMA lanes x 2 flops x the
-        # maximum SM clock (no measured FFMA peak exists for this machine)
+        # maximum SM clock (no measured FFMA peak is available)
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         mhz = clocks.get("sm_max_mhz") or 2070.0
         ffma_peak = sms * 128 * 2 * mhz * 1e6 / 1e12
