@@ -796,7 +796,7 @@ def run_gpu(args):
                  "path": "one cp_partial_attn_chunks per query block (no partials, no merge)"}
         del fstep
     backward = None
-    if w.dtype == "bf16" and not args.no_backward:
+    if not args.no_backward:
         # the backward of the same workload (f4), timed the same way (L2 flushed per step)
         if args.config == 4:
             bstep = UlyssesBwdStep(Step(4, dev))
@@ -821,8 +821,9 @@ def run_gpu(args):
         b_ach = bstep.flops / (b_kernel_ms * 1e-3) / 1e12
         backward = {"value": b_value, "unit": "TFLOP/s", "ms_per_step": b_ms,
                     "step_flop": bstep.flops, "flop_per_visible_pair": 10 * w.d * w.hq,
-                    "kernel": "attn_bwd_tc_kernel", "kernel_ms_per_step": b_kernel_ms,
-                    "achieved": b_ach, "peak": peaks["bf16"], "frac": b_ach / peaks["bf16"],
+                    "kernel": "attn_bwd_tc_kernel" if w.dtype == "bf16" else "bwd_simt_dkdv_kernel + bwd_simt_dq_kernel",
+                    "kernel_ms_per_step": b_kernel_ms, "achieved": b_ach,
+                    "peak": roofline["peak"], "frac": b_ach / roofline["peak"], "bound": roofline["bound"],
                     "launches_per_step": blaunch // args.steps,
                     "path": ("dO seq->head, per head-rank prep + full-sequence cp_partial_attn_bwd, "
                              "dQ and dK|dV head->seq (fp32); gradients zeroed in the step")
