@@ -385,7 +385,12 @@ class BwdStep:
         launches = 0
         for fn, kw in self.calls:
             fn(**kw)
-            launches += (len(kw["chunks"]) + 31) // 32 if "chunks" in kw else 1
+            fp32 = kw["q"].dtype == torch.float32  # CUDA-core path: two kernels per chunk
+            if "chunks" in kw:
+                live = sum(1 for c in kw["chunks"] if c[0].shape[0] > 0)
+                launches += 2 * live if fp32 else (live + 31) // 32
+            else:
+                launches += 2 if fp32 else 1
         if timers is not None:
             b = torch.cuda.Event(enable_timing=True)
             b.record(stream)
