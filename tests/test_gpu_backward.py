@@ -102,6 +102,9 @@ BWD_CASES = [
     (129, 129, 2, 1, 128, False, PosMap(0, 1), PosMap(0, 1), (64, PosMap(500, 1))),
     (200, 300, 2, 2, 128, True, PosMap(0, 1), PosMap(1000, 1), (200, PosMap(0, 1))),  # chunk in the future
     (1, 1, 1, 1, 64, True, PosMap(0, 1), PosMap(0, 1), None),
+    (700, 390, 16, 2, 64, False, PosMap(0, 1), PosMap(0, 1), (100, PosMap(390, 1))),  # GQA 8, ragged, non-causal
+    (257, 257, 1, 1, 128, True, PosMap(0, 1), PosMap(0, 1), None),                    # one head, ragged tails
+    (512, 1024, 8, 8, 128, True, PosMap(3, 2), PosMap(0, 1), (256, PosMap(2048, 1))),  # MHA, strided queries
 ]
 
 
