@@ -499,7 +499,7 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -635,7 +635,8 @@ def run_reference(args):
     w = wl.WORKLOADS[args.config]
     if world > 1 and rank != 0:
         return
-    rows = args.ref_rows or 64
+    # bounded: about 64 x 10 sampled rows over the whole timed run, whatever --steps is
+    rows = args.ref_rows or max(4, (64 * 10) // max(1, args.steps))
     for _ in range(args.warmup):
         oracle_sample(args.config, max(1, rows // 4), layout=args.layout)
     times, fl = [], 0
@@ -1023,14 +1024,14 @@ def run_pipelined(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--layout", default=None, choices=[None, "contiguous", "strided", "two_block"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--ref-rows", type=int, default=0,
-                    help="oracle sample rows (0: about 10 s of oracle work for the cpu baseline, "
-                         "64 per step for --impl reference)")
+                    help="oracle sample rows (0: about 10 s of oracle work for the cpu baseline; "
+                         "for --impl reference 640 rows spread over the timed steps, at least 4 per step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fused", action="store_true",
                     help="skip the extra measurement of the fused chunk-list path")
