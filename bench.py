@@ -571,6 +571,17 @@ def _blas_threads():
     return len(os.sched_getaffinity(0))
 
 
+_ORACLE_INPUTS = {}
+
+
+def _cached(key, make):
+    """Host copies of the sample's inputs, generated once per process (the timed steps of the
+    reference arm then time the oracle, not the input generation)."""
+    if key not in _ORACLE_INPUTS:
+        _ORACLE_INPUTS[key] = make()
+    return _ORACLE_INPUTS[key]
+
+
 def oracle_sample(cfg, rows_per_rank, seed=5, layout=None):
     """Time the CPU oracle on a bounded sample of the workload: for ``rows_per_rank`` seeded
     query rows, every chunk's partial then the merge.  Returns (seconds, causal-adjusted FLOPs,
@@ -587,8 +598,8 @@ def oracle_sample(cfg, rows_per_rank, seed=5, layout=None):
         S = w.seq_len
         hl, kl = w.hq // w.cp, w.hkv // w.cp
         q = wl.normal((rows_per_rank, hl, w.d), torch.bfloat16, 11, 0.5)
-        k = wl.normal((S, kl, w.d), torch.bfloat16, 12, 0.5)
-        v = wl.normal((S, kl, w.d), torch.bfloat16, 13, 0.5)
+        k = _cached((cfg, "k4"), lambda: wl.normal((S, kl, w.d), torch.bfloat16, 12, 0.5))
+        v = _cached((cfg, "v4"), lambda: wl.normal((S, kl, w.d), torch.bfloat16, 13, 0.5))
         rows = np.sort(np.random.default_rng(seed).choice(S, rows_per_rank, replace=False))
         t0 = time.perf_counter()
         oracle.attention(q, k, v, rows, np.arange(S), causal=True)
@@ -598,12 +609,12 @@ def oracle_sample(cfg, rows_per_rank, seed=5, layout=None):
     for qr in ranks:
         qpos = oracle.shard_positions(w.seq_len, w.cp, qr, layout)
         rows = wl.sample_rows(w.local_len, rows_per_rank, seed)
-        q = wl.shard_tensor(w, "q", qr, tokens=w.local_len)[rows]
+        q = _cached((cfg, "q", qr), lambda: wl.shard_tensor(w, "q", qr, tokens=w.local_len))[rows]
         parts = []
         for c in range(w.n_chunks):
             src, sub = divmod(c, w.chunks_per_shard)
-            k = wl.shard_tensor(w, "k", src)[sub * w.chunk_len:(sub + 1) * w.chunk_len]
-            v = wl.shard_tensor(w, "v", src)[sub * w.chunk_len:(sub + 1) * w.chunk_len]
+            k = _cached((cfg, "k", src), lambda: wl.shard_tensor(w, "k", src))[sub * w.chunk_len:(sub + 1) * w.chunk_len]
+            v = _cached((cfg, "v", src), lambda: wl.shard_tensor(w, "v", src))[sub * w.chunk_len:(sub + 1) * w.chunk_len]
             kpos = oracle.sub_chunk_positions(oracle.shard_positions(w.seq_len, w.cp, src, layout),
                                               sub, w.chunk_len)
             t0 = time.perf_counter()
