@@ -14,13 +14,46 @@ assignment -- every GPU gets both early and late tokens, so causal work is even.
 block-granular way to meet it (not printed on the pages; offered as an extra layout): cut the
 sequence into ``2 cp`` equal blocks and give rank ``r`` block ``r`` and block ``2 cp - 1 - r``,
 in that (ascending) order.
+
+Work-balanced contiguous split: "PCP and DCP sequence parallelism guide", section 2.3 (load
+balancing): an even split by token count leaves causal work uneven, since early tokens see
+only their prefix and late tokens see everything; DCP splits by the actual distribution of
+work instead.  Reading taken (the page gives no formula): contiguous blocks whose causal work is
+even at token granularity.  With ``W(b) = b (b + 1) / 2`` causal pairs among the first ``b``
+tokens, rank ``r`` holds ``[b_r, b_{r+1})`` where ``b_r`` is the smallest ``b`` with
+``W(b) >= r W(S) / cp`` (``b_0 = 0``, ``b_cp = S``); shards then have different lengths.
 """
+
+import math
 
 import numpy as np
 
 CONTIGUOUS = "contiguous"
 STRIDED = "strided"
 TWO_BLOCK = "two_block"
+BALANCED = "balanced"
+
+
+def balanced_bounds(seq_len: int, cp: int) -> list:
+    """Boundaries ``[b_0, ..., b_cp]`` of the work-balanced contiguous split (see the module
+    docstring).  Integer arithmetic: ``b_r`` is the smallest ``b`` with
+    ``b (b + 1) cp >= r S (S + 1)``."""
+    if cp <= 0 or seq_len <= 0:
+        raise ValueError("seq_len and cp must be positive")
+    total = seq_len * (seq_len + 1)
+    bounds = [0]
+    for r in range(1, cp):
+        need = r * total  # compare b (b + 1) cp against this
+        b = math.isqrt(need // cp)
+        while b > 0 and (b - 1) * b * cp >= need:
+            b -= 1
+        while b * (b + 1) * cp < need:
+            b += 1
+        bounds.append(b)
+    bounds.append(seq_len)
+    if any(bounds[i] >= bounds[i + 1] for i in range(cp)):
+        raise ValueError("the work-balanced split leaves a rank without tokens (seq_len too small for cp)")
+    return bounds
 
 
 def shard_positions(seq_len: int, cp: int, rank: int, kind: str) -> np.ndarray:
@@ -29,6 +62,9 @@ def shard_positions(seq_len: int, cp: int, rank: int, kind: str) -> np.ndarray:
         raise ValueError("seq_len and cp must be positive")
     if not 0 <= rank < cp:
         raise ValueError("rank out of range")
+    if kind == BALANCED:
+        bounds = balanced_bounds(seq_len, cp)
+        return np.arange(bounds[rank], bounds[rank + 1], dtype=np.int64)
     if seq_len % cp != 0:
         # the guide asserts divisibility; padding is the data pipeline's job
         raise ValueError("seq_len must be a multiple of cp")

@@ -268,9 +268,28 @@ def check_layouts(orc):
             work = orc.visible_pair_count(orc.shard_positions(seq_len, cp, r, "two_block"),
                                           np.arange(seq_len), True)
             assert work == b * b * (2 * cp - 1) + b * (b + 1), "two-block split is not balanced"
-    for kind in ("contiguous", "strided", "two_block"):
+    # work-balanced contiguous split: brute force over b (linear scan of the causal pair count
+    # W(b) = 1 + 2 + ... + b), and the balance it buys
+    for seq_len, cp in ((64, 4), (100, 3), (1000, 8), (4097, 5)):
+        total = seq_len * (seq_len + 1) // 2
+        bounds = [0]
+        for r in range(1, cp):
+            b, w = 0, 0
+            while w * cp < r * total:
+                b += 1
+                w += b
+            bounds.append(b)
+        bounds.append(seq_len)
+        for r in range(cp):
+            got = orc.shard_positions(seq_len, cp, r, "balanced")
+            assert list(got) == list(range(bounds[r], bounds[r + 1])), "balanced split differs from brute force"
+            work = orc.visible_pair_count(got, np.arange(seq_len), True)
+            assert abs(work - total / cp) <= seq_len, "balanced split is not balanced"
+    for kind in ("contiguous", "strided", "two_block", "balanced"):
         for seq_len, cp in ((64, 4), (48, 8), (7, 7), (14, 7), (32768, 8)):
             if kind == "two_block" and seq_len % (2 * cp):
+                continue
+            if kind == "balanced" and seq_len < 4 * cp:
                 continue
             allpos = np.concatenate([orc.shard_positions(seq_len, cp, r, kind) for r in range(cp)])
             assert np.array_equal(np.sort(allpos), np.arange(seq_len)), "layout is not a cover"

@@ -71,6 +71,10 @@ MUTANTS = [
     ("visible_strict", "layouts", 'side="right"', 'side="left"'),
     ("two_block_mirror", "layouts", "late = [(2 * cp - 1 - rank) * block + i",
      "late = [(cp + rank) * block + i"),
+    ("balanced_by_tokens", "layouts", "need = r * total  # compare b (b + 1) cp against this",
+     "need = r * seq_len * seq_len  # compare b (b + 1) cp against this"),
+    ("balanced_off_by_one", "layouts", "        while b * (b + 1) * cp < need:\n            b += 1\n        bounds.append(b)",
+     "        while b * (b + 1) * cp < need:\n            b += 1\n        bounds.append(b + 1)"),
     ("bwd_no_softmax_jacobian_term", "backward",
      "ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))", "ds = p * dp"),
     ("bwd_dq_unscaled", "backward", "dq[:, h, :] = scale * (ds @ k[:, g, :])",
