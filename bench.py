@@ -109,10 +109,15 @@ class Step:
             row = 0
             for m, n in cpa.shard_segments(w.seq_len, w.cp, src, self.layout):
                 step = min(w.chunk_len, n)
-                for sub in range(n // step):
-                    plan.append((src, row + sub * step, step, cpa.sub_chunk_map(m, sub, step)))
+                for lo in range(0, n, step):  # the last chunk of a segment may be shorter
+                    nk = min(step, n - lo)
+                    plan.append((src, row + lo, nk, cpa.PosMap(m.base + m.stride * lo, m.stride)))
                 row += n
         return plan
+
+    def shard_len(self, rank):
+        """Tokens rank `rank` holds (the workload's S/cp except for the balanced layout)."""
+        return sum(n for _, n in self.cpa.shard_segments(self.w.seq_len, self.w.cp, rank, self.layout))
 
     def _build_ranks(self, ranks):
         cpa, wl, w = self.cpa, self.wl, self.w
@@ -124,8 +129,8 @@ class Step:
         self._output_tensors = []
         self.pos_bufs = []
         for r in range(w.cp):
-            k = wl.shard_tensor(w, "k", r, device=dev)
-            v = wl.shard_tensor(w, "v", r, device=dev)
+            k = wl.shard_tensor(w, "k", r, device=dev, tokens=self.shard_len(r))
+            v = wl.shard_tensor(w, "v", r, device=dev, tokens=self.shard_len(r))
             kv[r] = (k, v)
             self._input_tensors += [k, v]
         self.kv = kv
@@ -135,12 +140,13 @@ class Step:
             # each affine segment of the query shard (one, or two for the two-block layout) is
             # its own query block: its partials, its merge (or its fused call)
             qsegs = cpa.shard_segments(w.seq_len, w.cp, qr, self.layout)
-            q = wl.shard_tensor(w, "q", qr, device=dev)
+            nloc = sum(n for _, n in qsegs)
+            q = wl.shard_tensor(w, "q", qr, device=dev, tokens=nloc)
             self._input_tensors.append(q)
-            self.pos_bufs.append((qr, torch.empty(w.local_len, dtype=torch.int32, device=dev)))
+            self.pos_bufs.append((qr, torch.empty(nloc, dtype=torch.int32, device=dev)))
             order = wl.arrival_order(len(plan), w.order_seed + 17 * qr)
-            out = torch.empty((w.local_len, w.hq, w.d), dtype=final_dtype, device=dev)
-            lse = torch.empty((w.local_len, w.hq), dtype=torch.float32, device=dev)
+            out = torch.empty((nloc, w.hq, w.d), dtype=final_dtype, device=dev)
+            lse = torch.empty((nloc, w.hq), dtype=torch.float32, device=dev)
             row = 0
             for qmap, nq in qsegs:
                 qs = q[row:row + nq]
@@ -608,19 +614,20 @@ def oracle_sample(cfg, rows_per_rank, seed=5, layout=None):
         return t, flops, f"{rows_per_rank} query rows x {hl} heads vs {S} keys (head-rank 0)"
     for qr in ranks:
         qpos = oracle.shard_positions(w.seq_len, w.cp, qr, layout)
-        rows = wl.sample_rows(w.local_len, rows_per_rank, seed)
-        q = _cached((cfg, "q", qr), lambda: wl.shard_tensor(w, "q", qr, tokens=w.local_len))[rows]
+        rows = wl.sample_rows(len(qpos), rows_per_rank, seed)
+        q = _cached((cfg, layout, "q", qr), lambda: wl.shard_tensor(w, "q", qr, tokens=len(qpos)))[rows]
         parts = []
-        for c in range(w.n_chunks):
-            src, sub = divmod(c, w.chunks_per_shard)
-            k = _cached((cfg, "k", src), lambda: wl.shard_tensor(w, "k", src))[sub * w.chunk_len:(sub + 1) * w.chunk_len]
-            v = _cached((cfg, "v", src), lambda: wl.shard_tensor(w, "v", src))[sub * w.chunk_len:(sub + 1) * w.chunk_len]
-            kpos = oracle.sub_chunk_positions(oracle.shard_positions(w.seq_len, w.cp, src, layout),
-                                              sub, w.chunk_len)
-            t0 = time.perf_counter()
-            parts.append(oracle.attention(q, k, v, qpos[rows], kpos, causal=w.causal))
-            t += time.perf_counter() - t0
-            flops += 4 * w.d * w.hq * oracle.visible_pair_count(qpos[rows], kpos, w.causal)
+        for src in range(w.cp):
+            spos = oracle.shard_positions(w.seq_len, w.cp, src, layout)
+            ks = _cached((cfg, layout, "k", src), lambda: wl.shard_tensor(w, "k", src, tokens=len(spos)))
+            vs = _cached((cfg, layout, "v", src), lambda: wl.shard_tensor(w, "v", src, tokens=len(spos)))
+            for lo in range(0, len(spos), w.chunk_len):
+                k, v = ks[lo:lo + w.chunk_len], vs[lo:lo + w.chunk_len]
+                kpos = spos[lo:lo + w.chunk_len]
+                t0 = time.perf_counter()
+                parts.append(oracle.attention(q, k, v, qpos[rows], kpos, causal=w.causal))
+                t += time.perf_counter() - t0
+                flops += 4 * w.d * w.hq * oracle.visible_pair_count(qpos[rows], kpos, w.causal)
         t0 = time.perf_counter()
         oracle.merge([p[0] for p in parts], [p[1] for p in parts])
         t += time.perf_counter() - t0
@@ -636,6 +643,9 @@ def _config_dict(w, layout, extra):
     if layout == "two_block" and w.chunk_len > w.local_len // 2:
         # a chunk never straddles the two blocks of a shard
         d.update(chunks=2 * w.cp, chunk_tokens=w.local_len // 2)
+    if layout == "balanced":
+        # shards of equal causal work, unequal length; each cut into chunks of at most chunk_tokens
+        d.update(chunks="per shard: ceil(shard tokens / chunk_tokens)")
     d.update(extra)
     return d
 
@@ -1038,7 +1048,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
-    ap.add_argument("--layout", default=None, choices=[None, "contiguous", "strided", "two_block"])
+    ap.add_argument("--layout", default=None, choices=[None, "contiguous", "strided", "two_block", "balanced"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--ref-rows", type=int, default=0,
                     help="oracle sample rows (0: about 10 s of oracle work for the cpu baseline; "

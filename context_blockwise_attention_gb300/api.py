@@ -14,7 +14,7 @@ import torch
 from . import build as _build
 
 CP_OK, CP_ERR_INVALID_ARG, CP_ERR_UNSUPPORTED, CP_ERR_CUDA, CP_ERR_TIMEOUT = range(5)
-CP_LAYOUT_CONTIGUOUS, CP_LAYOUT_STRIDED, CP_LAYOUT_TWO_BLOCK = 0, 1, 2
+CP_LAYOUT_CONTIGUOUS, CP_LAYOUT_STRIDED, CP_LAYOUT_TWO_BLOCK, CP_LAYOUT_BALANCED = 0, 1, 2, 3
 CP_MAX_SEGMENTS = 2
 CP_F32, CP_BF16 = 0, 1
 CP_FLAG_KV_DESCENDING = 0x1
@@ -23,8 +23,9 @@ CP_MAX_PARTIALS = 128
 CP_MAX_CHUNKS = 64
 
 _LAYOUTS = {"contiguous": CP_LAYOUT_CONTIGUOUS, "strided": CP_LAYOUT_STRIDED,
-            "two_block": CP_LAYOUT_TWO_BLOCK, CP_LAYOUT_CONTIGUOUS: CP_LAYOUT_CONTIGUOUS,
-            CP_LAYOUT_STRIDED: CP_LAYOUT_STRIDED, CP_LAYOUT_TWO_BLOCK: CP_LAYOUT_TWO_BLOCK}
+            "two_block": CP_LAYOUT_TWO_BLOCK, "balanced": CP_LAYOUT_BALANCED,
+            CP_LAYOUT_CONTIGUOUS: CP_LAYOUT_CONTIGUOUS, CP_LAYOUT_STRIDED: CP_LAYOUT_STRIDED,
+            CP_LAYOUT_TWO_BLOCK: CP_LAYOUT_TWO_BLOCK, CP_LAYOUT_BALANCED: CP_LAYOUT_BALANCED}
 
 
 class CpError(RuntimeError):
@@ -181,8 +182,9 @@ def shard_layout(seq_len, cp, rank, kind="contiguous", positions=False, device=N
 
 def shard_segments(seq_len, cp, rank, kind="contiguous", positions=False, device=None, stream=None):
     """The shard of rank ``rank`` as a list of ``(PosMap, length)`` affine segments in local
-    order (two for the two-block layout, one otherwise); with ``positions=True`` also an int32
-    CUDA tensor of every local token's position, filled by the library's kernel."""
+    order (two for the two-block layout, one otherwise; the balanced layout's shards differ in
+    length); with ``positions=True`` also an int32 CUDA tensor of every local token's position,
+    filled by the library's kernel."""
     lib = load_library()
     maps = (_PosMap * CP_MAX_SEGMENTS)()
     lens = (ctypes.c_int64 * CP_MAX_SEGMENTS)()
@@ -194,7 +196,7 @@ def shard_segments(seq_len, cp, rank, kind="contiguous", positions=False, device
         _check(lib.cp_shard_segments(int(seq_len), int(cp), int(rank), _LAYOUTS.get(kind, -1),
                                      maps, lens, ctypes.byref(n), None, None))
         device = device or torch.device("cuda", torch.cuda.current_device())
-        out = torch.empty(int(seq_len) // int(cp), dtype=torch.int32, device=device)
+        out = torch.empty(sum(int(lens[i]) for i in range(n.value)), dtype=torch.int32, device=device)
         ptr = ctypes.c_void_p(out.data_ptr())
     _check(lib.cp_shard_segments(int(seq_len), int(cp), int(rank), _LAYOUTS.get(kind, -1),
                                  maps, lens, ctypes.byref(n), ptr,

@@ -83,12 +83,42 @@ CP_API int32_t cp_version(void) { return CP_ABI_VERSION; }
 
 CP_API const char* cp_last_error(void) { return cpattn::g_err; }
 
+// Work-balanced split: the smallest b with b (b + 1) cp >= r S (S + 1), i.e. the first b whose
+// causal pair count W(b) = b (b + 1) / 2 reaches r / cp of the whole sequence's (b_0 = 0,
+// b_cp = S).  128-bit integers: r S (S + 1) exceeds 64 bits for long sequences.
+static int64_t balanced_bound(int64_t seq_len, int32_t cp, int32_t r) {
+  if (r <= 0) return 0;
+  if (r >= cp) return seq_len;
+  typedef unsigned __int128 u128;
+  const u128 need = static_cast<u128>(r) * static_cast<u128>(seq_len) * static_cast<u128>(seq_len + 1);
+  // start from the floating-point root, then step to the exact smallest b
+  int64_t b = static_cast<int64_t>(sqrtl(static_cast<long double>(need) / cp));
+  auto reach = [&](int64_t x) { return static_cast<u128>(x) * static_cast<u128>(x + 1) * static_cast<u128>(cp) >= need; };
+  while (b > 0 && reach(b - 1)) --b;
+  while (!reach(b)) ++b;
+  return b;
+}
+
 // The affine segments of rank `rank`'s shard under layout `kind`, in local order.
 static cp_status shard_segments(const char* who, int64_t seq_len, int32_t cp, int32_t rank,
                                 int32_t kind, cp_posmap* maps, int64_t* lens, int32_t* n) {
   if (seq_len <= 0) CP_INVALID("%s: seq_len must be positive (got %lld)", who, (long long)seq_len);
   if (cp <= 0) CP_INVALID("%s: cp must be positive (got %d)", who, cp);
   if (rank < 0 || rank >= cp) CP_INVALID("%s: rank %d not in [0, %d)", who, rank, cp);
+  if (kind == CP_LAYOUT_BALANCED) {
+    if (seq_len > (int64_t(1) << 40)) CP_INVALID("%s: seq_len too large for the balanced split", who);
+    const int64_t lo = balanced_bound(seq_len, cp, rank);
+    const int64_t hi = balanced_bound(seq_len, cp, rank + 1);
+    // every rank must hold tokens: the bounds must increase strictly
+    for (int32_t r = 0; r < cp; ++r)
+      if (balanced_bound(seq_len, cp, r) >= balanced_bound(seq_len, cp, r + 1))
+        CP_INVALID("%s: the balanced split of %lld tokens leaves rank %d of %d without tokens", who,
+                   (long long)seq_len, r, cp);
+    maps[0] = cp_posmap{lo, 1};
+    lens[0] = hi - lo;
+    *n = 1;
+    return CP_OK;
+  }
   if (seq_len % cp != 0)
     CP_INVALID("%s: seq_len %lld is not a multiple of cp %d", who, (long long)seq_len, cp);
   const int64_t local = seq_len / cp;
@@ -141,8 +171,8 @@ CP_API cp_status cp_shard_layout(int64_t seq_len, int32_t cp, int32_t rank, int3
   int32_t n = 0;
   cp_status st = shard_segments("cp_shard_layout", seq_len, cp, rank, kind, maps, lens, &n);
   if (st != CP_OK) return st;
-  if (n != 1)
-    CP_INVALID("cp_shard_layout: layout %d has %d affine segments; use cp_shard_segments", kind, n);
+  if (n != 1 || lens[0] * cp != seq_len)
+    CP_INVALID("cp_shard_layout: layout %d is not one map of seq_len/cp tokens; use cp_shard_segments", kind);
   st = fill_segments("cp_shard_layout", seq_len, maps, lens, n, dev_positions_out, stream);
   if (st != CP_OK) return st;
   *map_out = maps[0];

@@ -32,7 +32,7 @@
 extern "C" {
 #endif
 
-#define CP_ABI_VERSION 3
+#define CP_ABI_VERSION 4
 /* Largest number of partials one cp_merge_partials call accepts. */
 #define CP_MAX_PARTIALS 128
 
@@ -47,7 +47,8 @@ typedef enum {
 typedef enum {
   CP_LAYOUT_CONTIGUOUS = 0, /* one block of seq_len/cp tokens per rank                       */
   CP_LAYOUT_STRIDED = 1,    /* every cp-th token ("zig-zag" on the pages)                    */
-  CP_LAYOUT_TWO_BLOCK = 2   /* blocks r and 2cp-1-r of seq_len/(2cp) tokens (two segments)   */
+  CP_LAYOUT_TWO_BLOCK = 2,  /* blocks r and 2cp-1-r of seq_len/(2cp) tokens (two segments)   */
+  CP_LAYOUT_BALANCED = 3    /* contiguous blocks of equal causal work (unequal token counts) */
 } cp_layout;
 
 /* Most affine segments a shard layout has (cp_shard_segments). */
@@ -87,16 +88,25 @@ cp_status cp_shard_layout(int64_t seq_len, int32_t cp, int32_t rank, int32_t kin
  *     which the pages do not print: 2*cp blocks of b = seq_len/(2cp) tokens, rank r holds block r
  *     then block 2cp-1-r -- maps {r*b, 1} and {(2cp-1-r)*b, 1}, b tokens each.  Every rank then
  *     sees exactly b*b*(2cp-1) + b*(b+1) causal pairs.  Needs seq_len % (2*cp) == 0.
+ *   CP_LAYOUT_BALANCED: [PCP/DCP] section 2.3 (load balancing): an even split by tokens leaves
+ *     causal work uneven; DCP splits by the work instead.  Reading taken: contiguous blocks of
+ *     equal causal work at token granularity -- with W(b) = b(b+1)/2, rank r holds [b_r, b_r+1)
+ *     where b_r is the smallest b with W(b) >= r*W(seq_len)/cp (b_0 = 0, b_cp = seq_len).  One
+ *     segment per rank, lengths differ between ranks; seq_len need not divide by cp, but every
+ *     rank must get at least one token.
  * Arguments:
  *   seq_len, cp, rank, kind   as cp_shard_layout.
  *   maps_out, lens_out        host arrays [CP_MAX_SEGMENTS], required; entries past the count
  *                             are left untouched.
  *   n_segments_out            host pointer, required: 1 or 2.
- *   dev_positions_out         device int32 [seq_len/cp] or NULL: every local token's position,
- *                             written on `stream` (requires seq_len <= INT32_MAX).
+ *   dev_positions_out         device int32 [sum of lens] (seq_len/cp except for the balanced
+ *                             split) or NULL: every local token's position, written on `stream`
+ *                             (requires seq_len <= INT32_MAX).
  * Errors: CP_ERR_INVALID_ARG as cp_shard_layout (and seq_len % (2cp) != 0 for the two-block
- *         split); CP_ERR_CUDA if the fill kernel fails to launch.
- * cp_shard_layout rejects CP_LAYOUT_TWO_BLOCK (it is not one affine map).
+ *         split, a rank left without tokens for the balanced one); CP_ERR_CUDA if the fill
+ *         kernel fails to launch.
+ * cp_shard_layout rejects CP_LAYOUT_TWO_BLOCK and CP_LAYOUT_BALANCED (not one map of
+ * seq_len/cp tokens).  cp_ulysses_reshard needs equal shards and rejects CP_LAYOUT_BALANCED.
  */
 cp_status cp_shard_segments(int64_t seq_len, int32_t cp, int32_t rank, int32_t kind,
                             cp_posmap* maps_out, int64_t* lens_out, int32_t* n_segments_out,

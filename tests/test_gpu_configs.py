@@ -26,14 +26,15 @@ from context_blockwise_attention_gb300 import workloads as wl  # noqa: E402
 DEV = torch.device("cuda", 0) if torch.cuda.is_available() else None
 
 
-def _rows_for(w, n_rows, sample):
+def _rows_for(w, n_rows, sample, local=None):
+    local = w.local_len if local is None else local
     if sample is None:
-        return np.arange(w.local_len)
-    must = [0, w.local_len - 1, 127, 128, 255, 256, 383, 384]
+        return np.arange(local)
+    must = [0, local - 1, 127, 128, 255, 256, 383, 384]
     if w.chunks_per_shard > 1:
         for c in range(w.chunks_per_shard):
             must += [c * w.chunk_len, c * w.chunk_len - 1]
-    return wl.sample_rows(w.local_len, sample, seed=n_rows, must=must)
+    return wl.sample_rows(local, sample, seed=n_rows, must=must)
 
 
 def _check_rank_workload(cfg, layout, sample, query_ranks=None):
@@ -60,7 +61,7 @@ def _check_rank_workload(cfg, layout, sample, query_ranks=None):
     for step in steps:
         for qr, q, out, lse in step.rank_plans:
             qpos = shard_pos[qr]
-            rows = _rows_for(w, w.local_len + qr, sample)
+            rows = _rows_for(w, w.local_len + qr, sample, local=q.shape[0])
             q_cpu = q.cpu()
             # every partial on the sampled rows of its query block; positions from the oracle's
             # own layout, cut to the call's row ranges
@@ -104,7 +105,7 @@ def test_cfg2_rank0_sampled():
     _check_rank_workload(2, "strided", 256, query_ranks=[0])
 
 
-@pytest.mark.parametrize("layout", ["strided", "contiguous", "two_block"])
+@pytest.mark.parametrize("layout", ["strided", "contiguous", "two_block", "balanced"])
 def test_cfg3_all_ranks_sampled(layout):
     _check_rank_workload(3, layout, 128)
 
@@ -127,7 +128,7 @@ def _check_fused(cfg, layout, sample):
     all_pos = np.concatenate([oracle.shard_positions(w.seq_len, w.cp, r, layout) for r in range(w.cp)])
     for qr, q, out, lse in step.rank_plans:
         qpos = oracle.shard_positions(w.seq_len, w.cp, qr, layout)
-        rows = _rows_for(w, w.local_len + qr, sample)
+        rows = _rows_for(w, w.local_len + qr, sample, local=q.shape[0])
         idx = torch.from_numpy(rows).to(DEV)
         o_ref, l_ref = oracle.attention(q[idx].cpu(), all_k, all_v, qpos[rows], all_pos, causal=w.causal)
         compare_partial(out[idx].float().cpu().numpy(), lse[idx].cpu().numpy(), o_ref, l_ref,
@@ -137,6 +138,11 @@ def _check_fused(cfg, layout, sample):
 def test_cfg2_fused_full():
     # one launch consumes the 8 chunks in arrival order; every row and head
     _check_fused(2, "strided", None)
+
+
+def test_cfg3_balanced_fused_sampled():
+    # shards of equal causal work and unequal length, each query shard in one launch
+    _check_fused(3, "balanced", 128)
 
 
 def test_cfg3_two_block_fused_sampled():

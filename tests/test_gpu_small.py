@@ -130,8 +130,10 @@ def test_layout_positions_bit_exact(kind):
 
 
 def test_segments_positions_bit_exact():
-    for kind in ("contiguous", "strided", "two_block"):
+    for kind in ("contiguous", "strided", "two_block", "balanced"):
         for seq, cp in ((64, 4), (32768, 8), (131072, 4), (16, 8)):
+            if kind == "balanced" and seq < 4 * cp:
+                continue
             for r in range(cp):
                 segs, pos = cpa.shard_segments(seq, cp, r, kind, positions=True)
                 ref = oracle.shard_positions(seq, cp, r, kind)

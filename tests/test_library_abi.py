@@ -23,7 +23,7 @@ def test_exports_every_declared_function():
 
 
 def test_version():
-    assert cpa.version() == 3
+    assert cpa.version() == 4
 
 
 def test_desc_layout_matches_header():
@@ -188,8 +188,10 @@ def test_segments_host_maps_equal_oracle_positions():
     # host-only: the segments' affine maps, expanded, are the oracle's positions exactly
     import numpy as np
     import oracle
-    for kind_name, kind in (("contiguous", 0), ("strided", 1), ("two_block", 2)):
-        for seq, cp in ((64, 4), (48, 8), (32768, 8), (131072, 4), (16, 1)):
+    for kind_name, kind in (("contiguous", 0), ("strided", 1), ("two_block", 2), ("balanced", 3)):
+        for seq, cp in ((64, 4), (48, 8), (32768, 8), (131072, 4), (16, 1), (65537, 7)):
+            if kind != 3 and seq % (2 * cp if kind == 2 else cp):
+                continue
             for r in range(cp):
                 st, segs = _segments(seq, cp, r, kind)
                 assert st == 0
@@ -279,4 +281,15 @@ def test_bwd_chunks_rejects():
     arr[1].dv = 0x2000
     arr[1].kv_pos = api._PosMap(0, 0)
     assert lib.cp_partial_attn_bwd_chunks(ctypes.byref(d), 2, arr, None) == api.CP_ERR_INVALID_ARG
+
+
+def test_balanced_layout_rejects():
+    # too few tokens for every rank to get one; not one map of S/cp tokens; no Ulysses reshard
+    assert _segments(7, 7, 0, api.CP_LAYOUT_BALANCED)[0] == api.CP_ERR_INVALID_ARG
+    assert _layout(64, 4, 0, api.CP_LAYOUT_BALANCED)[0] == api.CP_ERR_INVALID_ARG
+    lib = cpa.load_library()
+    ptrs = (ctypes.c_void_p * 4)(0x1000, 0x2000, 0x3000, 0x4000)
+    heads = (ctypes.c_int32 * 1)(8)
+    assert lib.cp_ulysses_reshard(0, 4, 64, 1, heads, 64, 1, api.CP_LAYOUT_BALANCED, ptrs, ptrs,
+                                  None) == api.CP_ERR_INVALID_ARG
 
