@@ -18,6 +18,8 @@ from .api import (  # noqa: F401
     attn_bwd_prep,
     partial_attn_bwd,
     partial_attn_bwd_chunks,
+    partial_attn_bwd_noalloc,
+    NOALLOC_AUX_MAX_FLOATS,
     bwd_aux_floats,
     ulysses_reshard,
     library_path,
@@ -39,6 +41,8 @@ __all__ = [
     "attn_bwd_prep",
     "partial_attn_bwd",
     "partial_attn_bwd_chunks",
+    "partial_attn_bwd_noalloc",
+    "NOALLOC_AUX_MAX_FLOATS",
     "bwd_aux_floats",
     "ulysses_reshard",
     "library_path",

@@ -117,6 +117,8 @@ def load_library():
     lib.cp_partial_attn_bwd.argtypes = [ctypes.POINTER(_AttnBwdDesc), vp]
     lib.cp_partial_attn_bwd_chunks.restype = i32
     lib.cp_partial_attn_bwd_chunks.argtypes = [ctypes.POINTER(_AttnBwdDesc), i32, ctypes.POINTER(_KvBwdChunk), vp]
+    lib.cp_partial_attn_bwd_noalloc.restype = i32
+    lib.cp_partial_attn_bwd_noalloc.argtypes = [ctypes.POINTER(_AttnBwdDesc), vp, i32, vp, vp]
     lib.cp_merge_partials.restype = i32
     lib.cp_merge_partials.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), i64, i32, i32,
                                       vp, i32, vp, vp]
@@ -373,6 +375,56 @@ def partial_attn_bwd(q, k, v, d_o, aux, q_pos: PosMap, kv_pos: PosMap, dq, dk, d
     desc.wait_timeout_ms = int(wait_timeout_ms)
     desc.flags = int(flags)
     _check(lib.cp_partial_attn_bwd(ctypes.byref(desc), _stream(stream)))
+    return dq, dk, dv
+
+
+# Largest workspace partial_attn_bwd_noalloc can use (``CP_NOALLOC_AUX_MAX_FLOATS``).
+NOALLOC_AUX_MAX_FLOATS = 4194304
+
+
+def partial_attn_bwd_noalloc(q, k, v, d_o, o, lse, q_pos: PosMap, kv_pos: PosMap, dq, dk, dv, causal=True,
+                             scale=0.0, status=None, wait_timeout_ms=0, stream=None):
+    """``attn_bwd_prep`` and ``partial_attn_bwd`` in one call whose per-row workspace lives in the
+    library's own fixed device array, so that nothing is allocated: for callers that may not
+    allocate device memory.  ``o`` and ``lse`` are the shard's final output and LSE; the gradients
+    are accumulated into ``dq``, ``dk``, ``dv`` as by ``partial_attn_bwd``.  Calls that may overlap
+    on the GPU share the array and race; calls on one stream are safe.  Raises ``CpError`` when
+    ``bwd_aux_floats(Sq, Hq)`` is above ``NOALLOC_AUX_MAX_FLOATS``."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (d_o, "d_o"), (o, "o"), (lse, "lse"), (dq, "dq"), (dk, "dk"),
+                 (dv, "dv")):
+        _need_cuda(t, n)
+    if q.dim() != 3 or k.dim() != 3 or v.shape != k.shape or d_o.shape != q.shape or o.shape != q.shape:
+        raise CpError(CP_ERR_INVALID_ARG, "q, d_o, o must be [Sq, Hq, D]; k and v [Skv, Hkv, D]")
+    if not (q.dtype == k.dtype == v.dtype == d_o.dtype):
+        raise CpError(CP_ERR_INVALID_ARG, "q, k, v, d_o must share a dtype")
+    sq, hq, d = q.shape
+    skv, hkv, dk_ = k.shape
+    if dk_ != d:
+        raise CpError(CP_ERR_INVALID_ARG, "head_dim mismatch")
+    if tuple(lse.shape) != (sq, hq) or lse.dtype != torch.float32:
+        raise CpError(CP_ERR_INVALID_ARG, "lse must be fp32 [Sq, Hq]")
+    if dq.shape != q.shape or dk.shape != k.shape or dv.shape != k.shape or \
+            any(t.dtype != torch.float32 for t in (dq, dk, dv)):
+        raise CpError(CP_ERR_INVALID_ARG, "dq, dk, dv must be fp32 and shaped like q, k, v")
+    desc = _AttnBwdDesc()
+    desc.q, desc.k, desc.v, desc.d_o = q.data_ptr(), k.data_ptr(), v.data_ptr(), d_o.data_ptr()
+    desc.in_dtype = _dtype_code(q.dtype)
+    desc.aux = None
+    desc.dq, desc.dk, desc.dv = dq.data_ptr(), dk.data_ptr(), dv.data_ptr()
+    desc.sq, desc.skv, desc.hq, desc.hkv, desc.d = sq, skv, hq, hkv, d
+    desc.causal = 1 if causal else 0
+    desc.scale = float(scale)
+    desc.q_pos = _PosMap(q_pos.base, q_pos.stride)
+    desc.kv_pos = _PosMap(kv_pos.base, kv_pos.stride)
+    if status is not None:
+        _need_cuda(status, "status")
+        if status.dtype != torch.int32:
+            raise CpError(CP_ERR_INVALID_ARG, "status must be int32")
+        desc.status = status.data_ptr()
+    desc.wait_timeout_ms = int(wait_timeout_ms)
+    _check(lib.cp_partial_attn_bwd_noalloc(ctypes.byref(desc), ctypes.c_void_p(o.data_ptr()), _dtype_code(o.dtype),
+                                           ctypes.c_void_p(lse.data_ptr()), _stream(stream)))
     return dq, dk, dv
 
 

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(BUILD, "libcpattn.so")
 
 SOURCES = ["host.cu", "layout.cu", "merge.cu", "reshard.cu", "attn_simt.cu", "attn_tc.cu", "tmap.cu",
-           "bwd_prep.cu", "bwd_simt.cu", "bwd_tc.cu"]
+           "bwd_prep.cu", "bwd_simt.cu", "bwd_tc.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [
     "-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",

@@ -347,6 +347,37 @@ typedef struct {
 cp_status cp_partial_attn_bwd_chunks(const cp_attn_bwd_desc* desc, int32_t n_chunks,
                                      const cp_kv_bwd_chunk* chunks, cudaStream_t stream);
 
+/* Largest workspace (floats) cp_partial_attn_bwd_noalloc can use: CP_BWD_AUX_FLOATS(sq, hq) must
+ * not exceed it (16 MiB; e.g. 32768 rows x 64 heads, or 131072 rows x 16 heads). */
+#define CP_NOALLOC_AUX_MAX_FLOATS ((int64_t)4194304)
+
+/*
+ * cp_partial_attn_bwd_noalloc -- cp_attn_bwd_prep followed by cp_partial_attn_bwd for one
+ * (query shard, KV chunk) pair, with the per-row workspace held in the library's own device
+ * memory, so that the call allocates nothing.  The pages have no counterpart: this exists for
+ * callers that cannot allocate device memory themselves (a runtime that forbids cudaMalloc after
+ * start-up, code that runs inside a memory pool it does not own, a hook that is handed only its
+ * inputs and outputs).
+ * Arguments:
+ *   desc      as cp_partial_attn_bwd, except that desc->aux must be NULL; d_o is read with
+ *             desc->in_dtype by both steps
+ *   o, o_dtype, lse  as cp_attn_bwd_prep: the shard's final output and LSE
+ * dq, dk, dv are ACCUMULATED exactly as by cp_partial_attn_bwd (the caller zeroes them before the
+ * first call); nothing else needs to start at zero.
+ * The workspace is one fixed array of CP_NOALLOC_AUX_MAX_FLOATS floats per device, held by every
+ * device that loads the library until the process exits.  The first call on a device (with that
+ * device current) looks up the array's device address; make that first call before any stream
+ * capture.  Every call shares the array and leaves its contents behind: calls that may overlap on
+ * the GPU (different streams, or different host threads, without ordering between them) race on
+ * it and give wrong gradients.  Calls on one stream are ordered and safe.
+ * No cudaMalloc, cudaFree or other allocating call is made.
+ * Errors: CP_ERR_INVALID_ARG (desc NULL, desc->aux not NULL, CP_BWD_AUX_FLOATS(sq, hq) above
+ * CP_NOALLOC_AUX_MAX_FLOATS, and everything cp_attn_bwd_prep and cp_partial_attn_bwd reject),
+ * CP_ERR_UNSUPPORTED, CP_ERR_CUDA.
+ */
+cp_status cp_partial_attn_bwd_noalloc(const cp_attn_bwd_desc* desc, const void* o, int32_t o_dtype,
+                                      const float* lse, cudaStream_t stream);
+
 /* Message for the calling thread's last non-OK status ("" if none).  Valid until the next call. */
 const char* cp_last_error(void);
 
