@@ -1,0 +1,176 @@
+"""Seeded random sweeps of the partial, fused chunk-list and backward kernels against the oracle.
+
+The hand-picked cases elsewhere cover the named edge cases; these draw many more shapes at random
+(ragged row and key counts, GQA groups up to 8, both head dims, both input dtypes, affine position
+maps with strides 1..8 and offsets on either side of the queries, causal or not, default or
+explicit softmax scale), so that a tile-boundary or indexing slip that only shows for some
+combination has many chances to be caught.  Every draw comes from a fixed seed, and every case
+prints its parameters when it fails.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import helpers
+import oracle
+from helpers import TOL_BF16_LSE, TOL_BF16_O, TOL_F32, TOL_GRAD_BF16, TOL_GRAD_F32, compare_grad, compare_partial
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    helpers.ensure_built()
+
+import context_blockwise_attention_gb300 as cpa  # noqa: E402
+from context_blockwise_attention_gb300 import PosMap  # noqa: E402
+from context_blockwise_attention_gb300 import workloads as wl  # noqa: E402
+
+DEV = torch.device("cuda", 0) if torch.cuda.is_available() else None
+
+
+def _pos(m: PosMap, n):
+    return m.base + m.stride * np.arange(n, dtype=np.int64)
+
+
+def _draw_maps(rng, sq):
+    """A query map and a generator of KV maps placed before, across or after the queries."""
+    qs = int(rng.choice([1, 1, 2, 4, 8]))
+    qb = int(rng.integers(0, 3000))
+    q_end = qb + qs * max(sq - 1, 0)
+
+    def kv_map():
+        ks = int(rng.choice([1, 1, 2, 4, 8]))
+        kb = int(rng.integers(max(0, qb - 1500), q_end + 200))
+        return PosMap(kb, ks)
+
+    return PosMap(qb, qs), kv_map
+
+
+def _draw_heads(rng, d):
+    hkv = int(rng.choice([1, 2, 4]))
+    group = int(rng.choice([1, 2, 4, 8]))
+    if d == 128 and hkv * group > 8:
+        group = max(1, 8 // hkv)
+    return hkv * group, hkv
+
+
+def _draw_case(rng):
+    dtype = torch.bfloat16 if rng.random() < 0.7 else torch.float32
+    d = int(rng.choice([64, 128]))
+    hq, hkv = _draw_heads(rng, d)
+    sq = int(rng.integers(1, 600))
+    causal = bool(rng.random() < 0.75)
+    scale = 0.0 if rng.random() < 0.7 else float(rng.uniform(0.03, 0.2))
+    qm, kv_map = _draw_maps(rng, sq)
+    return dict(dtype=dtype, d=d, hq=hq, hkv=hkv, sq=sq, causal=causal, scale=scale, qm=qm, kv_map=kv_map)
+
+
+def _tols(dtype):
+    return (TOL_F32, TOL_F32) if dtype == torch.float32 else (TOL_BF16_O, TOL_BF16_LSE)
+
+
+N_PARTIAL = 40
+
+
+@pytest.mark.parametrize("i", range(N_PARTIAL), ids=[f"p{i}" for i in range(N_PARTIAL)])
+def test_random_partial(i):
+    rng = np.random.default_rng(5000 + i)
+    c = _draw_case(rng)
+    skv = int(rng.integers(1, 800))
+    km = c["kv_map"]()
+    seed = 7000 + 10 * i
+    q = wl.normal((c["sq"], c["hq"], c["d"]), c["dtype"], seed + 1, 0.5, device=DEV)
+    k = wl.normal((skv, c["hkv"], c["d"]), c["dtype"], seed + 2, 0.5, device=DEV)
+    v = wl.normal((skv, c["hkv"], c["d"]), c["dtype"], seed + 3, 1.0, device=DEV)
+    o = torch.full((c["sq"], c["hq"], c["d"]), float("nan"), device=DEV)
+    lse = torch.full((c["sq"], c["hq"]), float("nan"), device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    cpa.partial_attn(q, k, v, c["qm"], km, causal=c["causal"], o=o, lse=lse, status=status, scale=c["scale"])
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    o_ref, l_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), _pos(c["qm"], c["sq"]), _pos(km, skv),
+                                    causal=c["causal"], scale=c["scale"] if c["scale"] > 0 else None)
+    tol_o, tol_l = _tols(c["dtype"])
+    what = f"partial {i}: {({k_: c[k_] for k_ in c if k_ != 'kv_map'})} skv={skv} kv={km}"
+    compare_partial(o.cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, tol_o, tol_l, what)
+
+
+N_FUSED = 16
+
+
+@pytest.mark.parametrize("i", range(N_FUSED), ids=[f"f{i}" for i in range(N_FUSED)])
+def test_random_fused_chunks(i):
+    """One chunk-list call over 1..6 chunks (some empty) in a random arrival order."""
+    rng = np.random.default_rng(6000 + i)
+    c = _draw_case(rng)
+    n = int(rng.integers(1, 7))
+    seed = 8000 + 100 * i
+    q = wl.normal((c["sq"], c["hq"], c["d"]), c["dtype"], seed, 0.5, device=DEV)
+    chunks = []
+    for j in range(n):
+        skv = 0 if rng.random() < 0.1 else int(rng.integers(1, 500))
+        k = wl.normal((skv, c["hkv"], c["d"]), c["dtype"], seed + 10 * j + 1, 0.5, device=DEV)
+        v = wl.normal((skv, c["hkv"], c["d"]), c["dtype"], seed + 10 * j + 2, 1.0, device=DEV)
+        chunks.append((k, v, c["kv_map"]()))
+    order = [int(x) for x in rng.permutation(n)]
+    o = torch.full((c["sq"], c["hq"], c["d"]), float("nan"), device=DEV)
+    lse = torch.full((c["sq"], c["hq"]), float("nan"), device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    cpa.partial_attn_chunks(q, [chunks[j] for j in order], c["qm"], causal=c["causal"], o=o, lse=lse,
+                            status=status, scale=c["scale"])
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    k_all = torch.cat([ch[0].cpu() for ch in chunks])
+    v_all = torch.cat([ch[1].cpu() for ch in chunks])
+    pos = np.concatenate([_pos(ch[2], ch[0].shape[0]) for ch in chunks])
+    o_ref, l_ref = oracle.attention(q.cpu(), k_all, v_all, _pos(c["qm"], c["sq"]), pos, causal=c["causal"],
+                                    scale=c["scale"] if c["scale"] > 0 else None)
+    tol_o, tol_l = _tols(c["dtype"])
+    what = (f"fused {i}: {({k_: c[k_] for k_ in c if k_ != 'kv_map'})} order={order} "
+            f"chunks={[(ch[0].shape[0], ch[2]) for ch in chunks]}")
+    compare_partial(o.cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, tol_o, tol_l, what)
+
+
+N_BWD = 16
+
+
+@pytest.mark.parametrize("i", range(N_BWD), ids=[f"b{i}" for i in range(N_BWD)])
+def test_random_backward(i):
+    """Backward of one (query shard, chunk) pair whose rows' softmax also covers a second chunk,
+    against the oracle's chain rule with the final O and LSE over both chunks."""
+    rng = np.random.default_rng(9000 + i)
+    c = _draw_case(rng)
+    skv = int(rng.integers(1, 600))
+    km = c["kv_map"]()
+    oskv = int(rng.integers(0, 300))
+    okm = c["kv_map"]()
+    seed = 9500 + 10 * i
+    dt, sq, hq, hkv, d = c["dtype"], c["sq"], c["hq"], c["hkv"], c["d"]
+    q = wl.normal((sq, hq, d), dt, seed + 1, 0.5, device=DEV)
+    k = wl.normal((skv, hkv, d), dt, seed + 2, 0.5, device=DEV)
+    v = wl.normal((skv, hkv, d), dt, seed + 3, 1.0, device=DEV)
+    d_o = wl.normal((sq, hq, d), dt, seed + 4, 1.0, device=DEV)
+    k2 = wl.normal((oskv, hkv, d), dt, seed + 5, 0.5)
+    v2 = wl.normal((oskv, hkv, d), dt, seed + 6, 1.0)
+    scale = c["scale"] if c["scale"] > 0 else None
+    qp = _pos(c["qm"], sq)
+    o_ref, l_ref = oracle.attention(q.cpu(), torch.cat([k.cpu(), k2]), torch.cat([v.cpu(), v2]), qp,
+                                    np.concatenate([_pos(km, skv), _pos(okm, oskv)]), causal=c["causal"], scale=scale)
+    o32 = torch.from_numpy(o_ref).float()
+    l32 = torch.from_numpy(l_ref).float()
+    aux = cpa.attn_bwd_prep(o32.to(DEV), d_o, l32.to(DEV))
+    poison = 0.25
+    dq = torch.full(q.shape, poison, device=DEV)
+    dk = torch.full(k.shape, poison, device=DEV)
+    dv = torch.full(v.shape, poison, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    cpa.partial_attn_bwd(q, k, v, d_o, aux, c["qm"], km, dq, dk, dv, causal=c["causal"], scale=c["scale"],
+                         status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    ref = oracle.chunk_backward(q.cpu(), k.cpu(), v.cpu(), d_o.cpu(), o32, l32, qp, _pos(km, skv),
+                                causal=c["causal"], scale=scale)
+    tol = TOL_GRAD_BF16 if dt == torch.bfloat16 else TOL_GRAD_F32
+    what = f"bwd {i}: {({k_: c[k_] for k_ in c if k_ != 'kv_map'})} skv={skv} kv={km} other=({oskv}, {okm})"
+    for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        compare_grad(g.cpu().double().numpy() - poison, r, tol, f"{name} {what}")
