@@ -49,6 +49,8 @@ constexpr int kRows = 128;     // query rows per tile
 constexpr int kKeys = 128;     // keys per KV tile
 constexpr int kThreads = 384;  // 12 warps
 constexpr int kBwdMaxChunksPerLaunch = 32;  // chunk table size limit (kernel parameter space)
+constexpr int kJtBlock = 16;  // KV tiles of one head dealt together (blocked unit order)
+constexpr int kBlockedMinUnitsPerSm = 16;  // launches with fewer units keep the KV-tile-major order
 
 enum BwdSite : int {
   kSKvFull = 1,
@@ -75,7 +77,9 @@ struct BwdParams {
   int32_t hq, hkv, group, causal;
   int32_t n_qt;        // query tiles
   int32_t max_kt;      // KV tiles of the longest chunk
-  int64_t n_units;     // max_kt * n_chunks * hq
+  int32_t kt_blocks;   // blocks of kJtBlock KV tiles covering it
+  int32_t blocked;     // unit order: 0 KV-tile-major, 1 blocked (see decode_bunit)
+  int64_t n_units;     // (blocked ? kt_blocks * kJtBlock : max_kt) * n_chunks * hq
   float scale, sl2;    // scale, scale * log2(e)
   int64_t q_base, q_stride;
   int64_t timeout_ns;
@@ -133,12 +137,17 @@ static_assert(BLayout<128>::kSmemLaunch <= 232448, "shared memory budget (D=128)
 static_assert(BLayout<64>::kSmemLaunch <= 232448, "shared memory budget (D=64)");
 static_assert(BLayout<64>::kColDQ + 64 <= 512 && BLayout<128>::kColDK + 128 <= 512, "tensor memory budget");
 
-// Register split: 4 warps x 128 (TMA / MMA) + 4 x 248 (gradient) + 4 x 128 (reduction) =
-// 12 warps x 168, the launch's allocation.
-constexpr uint32_t kRegsControl = 128;
-constexpr uint32_t kRegsGrad = 248;
-constexpr uint32_t kRegsRed = 128;
-static_assert(4 * kRegsControl + 4 * kRegsGrad + 4 * kRegsRed == 12 * 168, "register split must match launch");
+// Register split (setmaxnreg), 12 warps x 168 at launch.  D = 128: 4 warps x 120 (TMA / MMA) +
+// 4 x 232 (gradient) + 4 x 152 (reduction: all four dQ boxes of a tile fit in registers, so the
+// dQ tensor-memory columns, which the next dP^T reuses, are released before any reduction is
+// issued).  D = 64: 4 x 128 + 4 x 248 + 4 x 128 (two dQ boxes; the gradient warps keep more).
+template <int D>
+struct BRegs {
+  static constexpr uint32_t kControl = (D == 128) ? 120 : 128;
+  static constexpr uint32_t kGrad = (D == 128) ? 232 : 248;
+  static constexpr uint32_t kRed = (D == 128) ? 152 : 128;
+  static_assert(4 * kControl + 4 * kGrad + 4 * kRed == 12 * 168, "register split must match launch");
+};
 
 struct Bars {
   uint32_t kv_full, kv_empty, q_full, q_empty, do_full, do_empty;  // q_*, do_*: stage 0, +8 per stage
@@ -152,17 +161,34 @@ struct BUnit {
   int nit;    // query tiles to visit (0: nothing to do)
 };
 
-// Units are (KV tile index, chunk, head) with the KV tile outermost: earliest keys first across
-// every chunk (they see the most query tiles), so the snake deal stays longest-first.  Tiles past
-// a shorter chunk's end are empty units.
+// Two unit orders.  KV-tile-major: (KV tile, chunk, head), earliest keys first across every
+// chunk -- unit lengths fall monotonically, which balances the snake deal best when a launch has
+// few rounds.  Blocked: (chunk, block of kJtBlock KV tiles, head, KV tile in the block) --
+// concurrent CTAs hold about 152 / kJtBlock heads with kJtBlock neighbouring KV tiles each, whose
+// walks start about a query tile apart and advance together, so each dQ tile they reduce into
+// and each Q and dO tile they read is touched by all of them within a short window while it is
+// in L2; in the KV-tile-major order those touches are spread over the whole launch and, once
+// the shard's fp32 dQ outgrows L2, most dQ reductions go to DRAM.  Blocks go earliest keys first,
+// so a launch still ends on a chunk's shortest units.  Tiles past a chunk's end are empty units.
 template <int MAXC>
 __device__ __forceinline__ BUnit decode_bunit(const BwdParams& p, const BwdChunks<MAXC>& ch, int64_t u) {
   BUnit w;
-  const int64_t per_tile = static_cast<int64_t>(ch.n) * p.hq;
-  w.jt = static_cast<int>(u / per_tile);
-  const int64_t rem = u - static_cast<int64_t>(w.jt) * per_tile;
-  w.c = static_cast<int>(rem / p.hq);
-  w.h = static_cast<int>(rem - static_cast<int64_t>(w.c) * p.hq);
+  if (p.blocked) {
+    const int64_t per_block = static_cast<int64_t>(kJtBlock) * p.hq;
+    const int64_t per_chunk = static_cast<int64_t>(p.kt_blocks) * per_block;
+    w.c = static_cast<int>(u / per_chunk);
+    int64_t rem = u - static_cast<int64_t>(w.c) * per_chunk;
+    const int jb = static_cast<int>(rem / per_block);
+    rem -= static_cast<int64_t>(jb) * per_block;
+    w.h = static_cast<int>(rem / kJtBlock);
+    w.jt = jb * kJtBlock + static_cast<int>(rem - static_cast<int64_t>(w.h) * kJtBlock);
+  } else {
+    const int64_t per_tile = static_cast<int64_t>(ch.n) * p.hq;
+    w.jt = static_cast<int>(u / per_tile);
+    const int64_t rem = u - static_cast<int64_t>(w.jt) * per_tile;
+    w.c = static_cast<int>(rem / p.hq);
+    w.h = static_cast<int>(rem - static_cast<int64_t>(w.c) * p.hq);
+  }
   w.g = w.h / p.group;
   w.t0 = 0;
   if (static_cast<int64_t>(w.jt) * kKeys >= ch.skv[w.c]) {
@@ -284,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sAux = sbase + L::kOffAux;
 
   if (warp < 4) {
-    ptx::regs_dec<kRegsControl>();
+    ptx::regs_dec<BRegs<D>::kControl>();
     if (warp == 0) {
       // ============================================================== TMA producer
       const bool leader = ptx::elect_one();
@@ -480,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp < 8) {
-    ptx::regs_inc<kRegsGrad>();
+    ptx::regs_inc<BRegs<D>::kGrad>();
     // ================================================================ gradient warpgroup
     const int wq = warp & 3;
     const int r = wq * 32 + lane;  // key row inside the KV tile
@@ -605,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    ptx::regs_dec<kRegsRed>();  // below the launch allocation: give registers back
+    ptx::regs_dec<BRegs<D>::kRed>();  // below the launch allocation: give registers back
     // ================================================================ reduction warpgroup
     const int wq = warp & 3;
     const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
@@ -623,22 +649,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = w.t0 + it;
         if (!(ok = wait_warp(b.dq_full, static_cast<uint32_t>(gi & 1), ctl, kSDqFull))) break;
         ptx::tc_fence_after();
-        // 64 columns at a time (registers); the tensor memory is released after the last read
+        // all of dQ into registers first, so the tensor memory goes back to the MMA warp (which
+        // at D = 128 puts the next dP^T there) before any reduction is issued
+        uint32_t v[D / 32][32];
 #pragma unroll
-        for (int c2 = 0; c2 < D / 64; ++c2) {
-          uint32_t v0[32], v1[32];
-          ptx::tmem_ld32(tmem + L::kColDQ + lane_bits + c2 * 64, v0);
-          ptx::tmem_ld32(tmem + L::kColDQ + lane_bits + c2 * 64 + 32, v1);
-          ptx::tmem_wait_ld();
-          if (c2 == D / 64 - 1) {
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(b.dq_free);
-          }
-          nred = reduce_box<L::kStageBufs>(stage0, lane, nred, v0, p.scale, &tm_dq, w.h * D + c2 * 64, t * kRows + wq * 32, p.sq);
-          nred = reduce_box<L::kStageBufs>(stage0, lane, nred, v1, p.scale, &tm_dq, w.h * D + c2 * 64 + 32, t * kRows + wq * 32,
-                            p.sq);
-        }
+        for (int c = 0; c < D / 32; ++c) ptx::tmem_ld32(tmem + L::kColDQ + lane_bits + c * 32, v[c]);
+        ptx::tmem_wait_ld();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(b.dq_free);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c)
+          nred = reduce_box<L::kStageBufs>(stage0, lane, nred, v[c], p.scale, &tm_dq, w.h * D + c * 32, t * kRows + wq * 32,
+                                           p.sq);
       }
       if (!ok) break;
       // end of the unit: dK (scaled) and dV
@@ -700,7 +723,9 @@ cp_status launch_bwd_dc(const BwdParams& p0, const cp_attn_bwd_desc& d, const cp
     if (kt > max_kt) max_kt = kt;
   }
   p.max_kt = static_cast<int32_t>(max_kt);
-  p.n_units = max_kt * n * d.hq;
+  p.kt_blocks = static_cast<int32_t>((max_kt + kJtBlock - 1) / kJtBlock);
+  p.blocked = (max_kt * n * d.hq >= static_cast<int64_t>(kBlockedMinUnitsPerSm) * num_sms) ? 1 : 0;
+  p.n_units = (p.blocked ? static_cast<int64_t>(p.kt_blocks) * kJtBlock : max_kt) * n * d.hq;
   CUtensorMap mq, mdo, mdq;
   const int64_t qe = int64_t(d.hq) * D;
   if (!encode_map_2d(&mq, d.q, d.sq, qe, false, 128) || !encode_map_2d(&mdo, d.d_o, d.sq, qe, false, 128) ||
@@ -753,6 +778,8 @@ cp_status launch_partial_attn_bwd_tc(const cp_attn_bwd_desc& d, const cp_kv_bwd_
   p.causal = d.causal;
   p.n_qt = static_cast<int32_t>((d.sq + kRows - 1) / kRows);
   p.max_kt = 0;
+  p.kt_blocks = 0;
+  p.blocked = 0;
   p.n_units = 0;
   p.scale = scale;
   p.sl2 = scale * 1.4426950408889634f;

@@ -323,3 +323,39 @@ def test_bwd_chunk_list_matches_oracle(dtype):
         compare_grad(dks[i].cpu().numpy(), bk, tol, f"chunk-list dK {i}")
         compare_grad(dvs[i].cpu().numpy(), bv, tol, f"chunk-list dV {i}")
     compare_grad(dq.cpu().numpy(), dq_ref, tol, "chunk-list dQ")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_chunk_list_blocked_order(d):
+    # enough units (KV tiles x chunks x heads >= 16 per SM) for the kernel to deal them in its
+    # blocked order -- 16 KV tiles of a head together -- with chunks of 20 KV tiles (so blocks
+    # run past a chunk's end), a ragged last tile, a chunk in the future and GQA 4
+    sq, hq, hkv = 300, 16, 4
+    qm = PosMap(20000, 7)
+    specs = [(2560, PosMap(j, 8)) for j in range(7)] + [(2500, PosMap(7, 8)), (2560, PosMap(10 ** 6, 1))]
+    assert sum(-(-n // 128) for n, _ in specs[:8]) * hq >= 16 * 152
+    q = wl.normal((sq, hq, d), torch.bfloat16, 191, 0.5, device=DEV)
+    d_o = wl.normal((sq, hq, d), torch.bfloat16, 192, 1.0, device=DEV)
+    ks = [wl.normal((n, hkv, d), torch.bfloat16, 193 + i, 0.5, device=DEV) for i, (n, _) in enumerate(specs)]
+    vs = [wl.normal((n, hkv, d), torch.bfloat16, 213 + i, 1.0, device=DEV) for i, (n, _) in enumerate(specs)]
+    kpos = np.concatenate([_pos(m, n) for n, m in specs])
+    o_ref, l_ref = oracle.attention(q.cpu(), torch.cat([k.cpu() for k in ks]), torch.cat([v.cpu() for v in vs]),
+                                    _pos(qm, sq), kpos, causal=True)
+    o32, l32 = torch.from_numpy(o_ref).float(), torch.from_numpy(l_ref).float()
+    aux = cpa.attn_bwd_prep(o32.to(DEV), d_o, l32.to(DEV))
+    dq = torch.zeros(q.shape, device=DEV)
+    dks = [torch.zeros(k.shape, device=DEV) for k in ks]
+    dvs = [torch.zeros(k.shape, device=DEV) for k in ks]
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    cpa.partial_attn_bwd_chunks(q, d_o, aux, qm, [(k, v, m, dk, dv) for k, v, (_, m), dk, dv in
+                                                   zip(ks, vs, specs, dks, dvs)], dq, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    dq_ref = np.zeros((sq, hq, d))
+    for i, (n, m) in enumerate(specs):
+        a, bk, bv = oracle.chunk_backward(q.cpu(), ks[i].cpu(), vs[i].cpu(), d_o.cpu(), o32, l32, _pos(qm, sq),
+                                          _pos(m, n), causal=True)
+        dq_ref += a
+        compare_grad(dks[i].cpu().numpy(), bk, TOL_GRAD_BF16, f"blocked dK {i}")
+        compare_grad(dvs[i].cpu().numpy(), bv, TOL_GRAD_BF16, f"blocked dV {i}")
+    compare_grad(dq.cpu().numpy(), dq_ref, TOL_GRAD_BF16, "blocked dQ")
