@@ -11,14 +11,17 @@
 // How (GB300 design):
 //   * Persistent, one CTA per SM.  A unit is one 128-key KV tile of one Q head; it walks every
 //     128-row query tile that can see the KV tile (causal: tiles whose last row's position is at
-//     least the tile's first key position).  Units are numbered earliest keys first (they see
-//     the most query tiles) and dealt round by round in snake order.
+//     least the tile's first key position).  Units are dealt round by round in snake order, in
+//     one of two orders (decode_bunit): earliest keys first across the call's chunks for small
+//     launches, or chunk by chunk in blocks of 16 KV tiles of one head for large ones, which keeps
+//     the dQ tiles a head's units reduce into resident in L2.
 //   * warp 0: TMA producer (K, V once per unit; Q, dO tiles and the rows' -LSE*log2(e), -D runs
 //     per query tile).  warp 1: allocates tensor memory, issues tcgen05.mma (whole warp waits,
 //     one elected lane issues).  warps 4-7: gradient warpgroup, one thread per key row -- turns
 //     S^T into P^T and dP^T into dS^T.  warps 8-11: reduction warpgroup -- adds dQ (per query
-//     tile) and dK, dV (per unit) into global memory with TMA bulk reductions (fp32 add), so
-//     concurrent CTAs and GQA heads accumulate without a separate pass.
+//     tile; all of a tile's dQ is read from tensor memory before the first reduction) and dK, dV
+//     (per unit) into global memory with TMA bulk reductions (fp32 add), so concurrent CTAs and
+//     GQA heads accumulate without a separate pass.
 //   * Tensor memory: S^T (128 fp32 columns, P^T bf16 written over its first 64), dP^T (128,
 //     dS^T bf16 over its first 64), dV and dK accumulators (D each), dQ (D; for D = 128 it
 //     reuses the dP^T columns once the dK product has consumed dS^T).
