@@ -174,3 +174,41 @@ def test_random_backward(i):
     what = f"bwd {i}: {({k_: c[k_] for k_ in c if k_ != 'kv_map'})} skv={skv} kv={km} other=({oskv}, {okm})"
     for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
         compare_grad(g.cpu().double().numpy() - poison, r, tol, f"{name} {what}")
+
+
+# head-count extremes the random draws do not reach: MQA with many query heads, wide GQA at D=128
+_HEAD_CASES = [(64, 1, 64), (16, 1, 128), (64, 8, 128), (1, 1, 128)]
+
+
+@pytest.mark.parametrize("hq,hkv,d", _HEAD_CASES, ids=[f"h{a}_{b}_d{c}" for a, b, c in _HEAD_CASES])
+def test_head_extremes(hq, hkv, d):
+    sq, skv = 200, 333
+    qm, km, km2 = PosMap(100, 3), PosMap(0, 2), PosMap(1, 2)
+    q = wl.normal((sq, hq, d), torch.bfloat16, 11, 0.5, device=DEV)
+    k = wl.normal((skv, hkv, d), torch.bfloat16, 12, 0.5, device=DEV)
+    v = wl.normal((skv, hkv, d), torch.bfloat16, 13, 1.0, device=DEV)
+    k2 = wl.normal((150, hkv, d), torch.bfloat16, 14, 0.5, device=DEV)
+    v2 = wl.normal((150, hkv, d), torch.bfloat16, 15, 1.0, device=DEV)
+    d_o = wl.normal((sq, hq, d), torch.bfloat16, 16, 1.0, device=DEV)
+    qp = _pos(qm, sq)
+    # forward, one chunk
+    o, lse = cpa.partial_attn(q, k, v, qm, km, causal=True)
+    o_ref, l_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), qp, _pos(km, skv), causal=True)
+    compare_partial(o.cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, TOL_BF16_O, TOL_BF16_LSE, f"partial {hq}/{hkv}")
+    # forward over both chunks in one call
+    o2, l2 = cpa.partial_attn_chunks(q, [(k2, v2, km2), (k, v, km)], qm, causal=True)
+    kall, vall = torch.cat([k.cpu(), k2.cpu()]), torch.cat([v.cpu(), v2.cpu()])
+    kp = np.concatenate([_pos(km, skv), _pos(km2, 150)])
+    o2_ref, l2_ref = oracle.attention(q.cpu(), kall, vall, qp, kp, causal=True)
+    compare_partial(o2.cpu().numpy(), l2.cpu().numpy(), o2_ref, l2_ref, TOL_BF16_O, TOL_BF16_LSE, f"chunks {hq}/{hkv}")
+    # backward of the first chunk against the final (two-chunk) O and LSE
+    o32, l32 = torch.from_numpy(o2_ref).float(), torch.from_numpy(l2_ref).float()
+    aux = cpa.attn_bwd_prep(o32.to(DEV), d_o, l32.to(DEV))
+    dq = torch.zeros(q.shape, device=DEV)
+    dk = torch.zeros(k.shape, device=DEV)
+    dv = torch.zeros(v.shape, device=DEV)
+    cpa.partial_attn_bwd(q, k, v, d_o, aux, qm, km, dq, dk, dv, causal=True)
+    torch.cuda.synchronize()
+    ref = oracle.chunk_backward(q.cpu(), k.cpu(), v.cpu(), d_o.cpu(), o32, l32, qp, _pos(km, skv), causal=True)
+    for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        compare_grad(g.cpu().numpy(), r, TOL_GRAD_BF16, f"{name} {hq}/{hkv} d={d}")
