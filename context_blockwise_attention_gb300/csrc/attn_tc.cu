@@ -110,8 +110,11 @@ struct Layout {
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffStage = kOffV + kStages * kTileBytes;  // 16 KB box per warpgroup
-  static constexpr int kOffBar = kOffStage + 2 * kChunkBytes;
+  // 16 KB staging boxes per warpgroup: two at D = 64 (shared memory has room; an fp32 O tile is
+  // two boxes, so neither waits for the other's bulk store), one at D = 128
+  static constexpr int kStageBufs = (D == 64) ? 2 : 1;
+  static constexpr int kOffStage = kOffV + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffStage + 2 * kStageBufs * kChunkBytes;
   // barriers: q_full, q_empty, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2],
   //           p_half[2], p_full[2], o_final[2], o_empty[2], never, drain
   static constexpr int kNumBars = 2 + 4 * kStages + 10 + 2;
@@ -122,6 +125,7 @@ struct Layout {
   static constexpr int kBoxesBf16 = D / 64;          // 64 bf16 columns per box
 };
 static_assert(Layout<128>::kSmemLaunch <= 232448, "shared memory budget (D=128)");
+static_assert(Layout<64>::kSmemLaunch <= 232448, "shared memory budget (D=64)");
 
 // Register split (setmaxnreg): the TMA/MMA warpgroup gives registers to the two softmax
 // warpgroups.  4 warps x 120 + 8 warps x 192 = 12 warps x 168, the launch's allocation (measured
@@ -470,14 +474,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_bits = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + x * 128u + lane_bits;
     const uint32_t tO = tmem + 256u + x * 128u + lane_bits;
-    const uint32_t stage = sbase + L::kOffStage + static_cast<uint32_t>(x) * L::kChunkBytes;
-    const uint32_t row_addr = stage + static_cast<uint32_t>(r) * 128u;
+    const uint32_t stage0 = sbase + L::kOffStage + static_cast<uint32_t>(x * L::kStageBufs) * L::kChunkBytes;
     const uint32_t sw = static_cast<uint32_t>(r & 7);
     const bool store_leader = (wq == 0 && lane == 0);
     const float sl2 = p.scale_log2;
     const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
     bool ok = true;
     bool staged = false;  // a bulk store from the staging box may still be reading it
+    uint32_t nbox = 0;    // staging boxes written so far (every thread of the warpgroup counts)
     int64_t g = 0, kq = 0;
 
     for (int64_t k = 0;; ++k) {
@@ -606,8 +610,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv = has ? 1.0f / l : 0.0f;
       const int boxes = p.o_bf16 ? L::kBoxesBf16 : L::kBoxesF32;
       for (int c = 0; c < boxes; ++c) {
-        // the staging box is reusable once the previous bulk store has finished reading it
-        if (staged && store_leader) ptx::bulk_wait_read_all();
+        // boxes rotate through the staging buffers across units (one bulk group per box), so the
+        // box is reusable once the bulk store kStageBufs boxes back has finished reading it
+        const uint32_t stage = stage0 + (nbox % L::kStageBufs) * L::kChunkBytes;
+        const uint32_t row_addr = stage + static_cast<uint32_t>(r) * 128u;
+        ++nbox;
+        if (staged && store_leader) {
+          if (L::kStageBufs == 2)
+            ptx::bulk_wait_read<1>();
+          else
+            ptx::bulk_wait_read_all();
+        }
         ptx::named_bar_sync(1 + x, 128);
         if (p.o_bf16) {
           // box = 64 bf16 columns = O chunks 2c, 2c+1; 16-byte chunk q holds columns 8q..8q+7
