@@ -17,7 +17,8 @@
  *   - Tensors are token-major, batch 1: [tokens, heads, head_dim], contiguous, head_dim fastest.
  *   - Global positions are affine per shard: pos(i) = base + stride * i, stride >= 1.
  *   - All device pointers are caller-owned device memory; the library allocates no device memory
- *     and keeps no state between calls.  Host pointer arrays are read during the call only.
+ *     and keeps no state between calls (one exception: the fixed workspace array behind
+ *     cp_partial_attn_bwd_noalloc).  Host pointer arrays are read during the call only.
  *   - Every call is asynchronous on `stream` (0 = legacy default stream).  Argument checks run on
  *     the host before anything is launched; a rejected call launches nothing.
  *   - On a non-OK status, cp_last_error() returns a message for the calling thread.
@@ -141,8 +142,12 @@ cp_status cp_shard_segments(int64_t seq_len, int32_t cp, int32_t rank, int32_t k
  *             The caller zeroes it; read it after synchronising.
  *   flags     CP_FLAG_* bits
  *   wait_timeout_ms  limit of each in-kernel wait; 0 means 2000 ms
- * Errors: CP_ERR_INVALID_ARG (null pointers, d not 64/128, hq % hkv, stride < 1, bad dtype,
- * pointers not 16-byte aligned), CP_ERR_UNSUPPORTED (device not sm_103), CP_ERR_CUDA.
+ * Positions: base >= 0, stride >= 1, and every global position of the shard and of the chunk
+ * below 2e9 (a checked limit that keeps positions within the int32 position arrays of the layout
+ * calls; far beyond any sequence length).
+ * Errors: CP_ERR_INVALID_ARG (null pointers, d not 64/128, hq % hkv, stride < 1, negative base,
+ * positions at or above 2e9, bad dtype, pointers not 16-byte aligned), CP_ERR_UNSUPPORTED
+ * (device not sm_103), CP_ERR_CUDA.
  */
 typedef struct {
   const void* q;
@@ -298,6 +303,7 @@ cp_status cp_attn_bwd_prep(const void* o, int32_t o_dtype, const void* d_o, int3
  * Within one call dq, dk, dv are updated with atomic reductions (bf16 path) or by exclusive
  * owners (fp32 path); calls on one stream follow stream order.  The summation order of dq and
  * of a GQA group's dk, dv is not fixed on the bf16 path.
+ * Positions as cp_partial_attn (every global position below 2e9).
  * Errors: CP_ERR_INVALID_ARG, CP_ERR_UNSUPPORTED, CP_ERR_CUDA.
  */
 typedef struct {

@@ -212,3 +212,41 @@ def test_head_extremes(hq, hkv, d):
     ref = oracle.chunk_backward(q.cpu(), k.cpu(), v.cpu(), d_o.cpu(), o32, l32, qp, _pos(km, skv), causal=True)
     for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
         compare_grad(g.cpu().numpy(), r, TOL_GRAD_BF16, f"{name} {hq}/{hkv} d={d}")
+
+
+def test_positions_near_the_limit():
+    """Positions up to just below the checked limit (2e9) with strides in the millions: the
+    kernels' position arithmetic (products of a stride and a row index near 2^31, differences of
+    large positions) matches the oracle on the same int64 positions, in the partial, the chunk
+    list and the backward."""
+    sq, hq, hkv, d = 333, 4, 2, 128
+    qm = PosMap(7, 6_000_000)
+    specs = [(300, PosMap(3, 6_000_000)), (257, PosMap(1_794_000_005, 777))]
+    q = wl.normal((sq, hq, d), torch.bfloat16, 41, 0.5, device=DEV)
+    d_o = wl.normal((sq, hq, d), torch.bfloat16, 42, 1.0, device=DEV)
+    ks = [wl.normal((n, hkv, d), torch.bfloat16, 43 + i, 0.5, device=DEV) for i, (n, _) in enumerate(specs)]
+    vs = [wl.normal((n, hkv, d), torch.bfloat16, 53 + i, 1.0, device=DEV) for i, (n, _) in enumerate(specs)]
+    qp = _pos(qm, sq)
+    kp = [_pos(m, n) for n, m in specs]
+    assert qp.max() > 1.99e9 and max(k.max() for k in kp) < 2e9 and qp.max() < 2e9
+    o1, l1 = cpa.partial_attn(q, ks[1], vs[1], qm, specs[1][1], causal=True)
+    r1 = oracle.attention(q.cpu(), ks[1].cpu(), vs[1].cpu(), qp, kp[1], causal=True)
+    compare_partial(o1.cpu().numpy(), l1.cpu().numpy(), *r1, TOL_BF16_O, TOL_BF16_LSE, "partial, positions near 2e9")
+    o, lse = cpa.partial_attn_chunks(q, [(ks[i], vs[i], specs[i][1]) for i in (1, 0)], qm, causal=True)
+    ref_o, ref_l = oracle.attention(q.cpu(), torch.cat([k.cpu() for k in ks]), torch.cat([v.cpu() for v in vs]),
+                                    qp, np.concatenate(kp), causal=True)
+    compare_partial(o.cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l, TOL_BF16_O, TOL_BF16_LSE, "chunks, positions near 2e9")
+    o32, l32 = torch.from_numpy(ref_o).float(), torch.from_numpy(ref_l).float()
+    aux = cpa.attn_bwd_prep(o32.to(DEV), d_o, l32.to(DEV))
+    dq = torch.zeros(q.shape, device=DEV)
+    dks = [torch.zeros(k.shape, device=DEV) for k in ks]
+    dvs = [torch.zeros(k.shape, device=DEV) for k in ks]
+    cpa.partial_attn_bwd_chunks(q, d_o, aux, qm, [(ks[i], vs[i], specs[i][1], dks[i], dvs[i]) for i in (0, 1)], dq)
+    torch.cuda.synchronize()
+    dq_ref = np.zeros((sq, hq, d))
+    for i in range(2):
+        a, bk, bv = oracle.chunk_backward(q.cpu(), ks[i].cpu(), vs[i].cpu(), d_o.cpu(), o32, l32, qp, kp[i], causal=True)
+        dq_ref += a
+        compare_grad(dks[i].cpu().numpy(), bk, TOL_GRAD_BF16, f"dK {i}, positions near 2e9")
+        compare_grad(dvs[i].cpu().numpy(), bv, TOL_GRAD_BF16, f"dV {i}, positions near 2e9")
+    compare_grad(dq.cpu().numpy(), dq_ref, TOL_GRAD_BF16, "dQ, positions near 2e9")

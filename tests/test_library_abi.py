@@ -83,6 +83,8 @@ def _desc(**kw):
     ("q", 0), ("k", 0), ("o", 0), ("lse", 0), ("q", 0x1008), ("sq", -1), ("flags", 0x40),
     ("q_pos", api._PosMap(0, 0)), ("kv_pos", api._PosMap(-5, 1)), ("scale", -1.0),
     ("wait_timeout_ms", -3),
+    # global positions must stay below 2e9: the shard's last position, then the chunk's
+    ("q_pos", api._PosMap(2_000_000_000 - 100, 1)), ("kv_pos", api._PosMap(7, 16_000_000)),
 ])
 def test_partial_attn_rejects(field, value):
     lib = cpa.load_library()
