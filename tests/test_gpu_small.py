@@ -365,3 +365,26 @@ def test_fused_all_chunks_empty():
     o, l = cpa.partial_attn_chunks(q, [(e, e, PosMap(0, 1)), (e, e, PosMap(9, 1))], PosMap(0, 1))
     torch.cuda.synchronize()
     assert torch.all(o == 0) and torch.all(torch.isneginf(l))
+
+
+@pytest.mark.parametrize("kind", ["contiguous", "strided", "two_block"])
+@pytest.mark.parametrize("cp", [1, 64])
+def test_reshard_extreme_cp_and_four_tensors(cp, kind):
+    # the API's extremes: one rank, and 64 ranks with one head each (a 128-byte run per token);
+    # four tensors in one launch, both directions, bit-exact against the oracle's index formula
+    seq, d = 1024, 64
+    heads = (64, 64, 128, 64)
+    shards = [[wl.normal((seq // cp, hh, d), torch.bfloat16, 700 + 10 * t + r, device=DEV) for r in range(cp)]
+              for t, hh in enumerate(heads)]
+    pos = [oracle.shard_positions(seq, cp, r, kind) for r in range(cp)]
+    ys = cpa.ulysses_reshard("seq_to_head", shards, cp, seq, kind)
+    torch.cuda.synchronize()
+    for t in range(4):
+        ref = oracle.seq_to_head([x.cpu().view(torch.int16).numpy() for x in shards[t]], pos)
+        for r in range(cp):
+            assert np.array_equal(ys[t][r].cpu().view(torch.int16).numpy(), ref[r]), (t, r)
+    back = cpa.ulysses_reshard("head_to_seq", ys, cp, seq, kind)
+    torch.cuda.synchronize()
+    for t in range(4):
+        for r in range(cp):
+            assert torch.equal(back[t][r], shards[t][r]), (t, r)
