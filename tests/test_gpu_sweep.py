@@ -250,3 +250,44 @@ def test_positions_near_the_limit():
         compare_grad(dks[i].cpu().numpy(), bk, TOL_GRAD_BF16, f"dK {i}, positions near 2e9")
         compare_grad(dvs[i].cpu().numpy(), bv, TOL_GRAD_BF16, f"dV {i}, positions near 2e9")
     compare_grad(dq.cpu().numpy(), dq_ref, TOL_GRAD_BF16, "dQ, positions near 2e9")
+
+
+def test_chunk_lists_at_the_maximum():
+    """CP_MAX_CHUNKS = 64 small chunks (ragged, some empty, strided positions) in one forward call,
+    and the same 64 in one backward call, which the library splits into launches of at most 32
+    chunks (the 32-chunk and the 8-chunk table sizes both run)."""
+    sq, hq, hkv, d = 260, 4, 2, 64
+    rng = np.random.default_rng(77)
+    qm = PosMap(5, 8)
+    specs = []
+    for i in range(cpa.api.CP_MAX_CHUNKS):
+        n = 0 if i % 9 == 4 else int(rng.integers(1, 40))
+        specs.append((n, PosMap(int(rng.integers(0, 2400)), int(rng.choice([1, 4, 8])))))
+    q = wl.normal((sq, hq, d), torch.bfloat16, 61, 0.5, device=DEV)
+    d_o = wl.normal((sq, hq, d), torch.bfloat16, 62, 1.0, device=DEV)
+    ks = [wl.normal((n, hkv, d), torch.bfloat16, 1000 + i, 0.5, device=DEV) for i, (n, _) in enumerate(specs)]
+    vs = [wl.normal((n, hkv, d), torch.bfloat16, 2000 + i, 1.0, device=DEV) for i, (n, _) in enumerate(specs)]
+    qp = _pos(qm, sq)
+    kp = np.concatenate([_pos(m, n) for n, m in specs])
+    o, lse = cpa.partial_attn_chunks(q, [(ks[i], vs[i], specs[i][1]) for i in range(len(specs))], qm, causal=True)
+    ref_o, ref_l = oracle.attention(q.cpu(), torch.cat([k.cpu() for k in ks]), torch.cat([v.cpu() for v in vs]),
+                                    qp, kp, causal=True)
+    compare_partial(o.cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l, TOL_BF16_O, TOL_BF16_LSE, "64-chunk forward")
+    o32, l32 = torch.from_numpy(ref_o).float(), torch.from_numpy(ref_l).float()
+    aux = cpa.attn_bwd_prep(o32.to(DEV), d_o, l32.to(DEV))
+    dq = torch.zeros(q.shape, device=DEV)
+    dks = [torch.zeros(k.shape, device=DEV) for k in ks]
+    dvs = [torch.zeros(k.shape, device=DEV) for k in ks]
+    cpa.partial_attn_bwd_chunks(q, d_o, aux, qm, [(ks[i], vs[i], specs[i][1], dks[i], dvs[i]) for i in range(len(specs))],
+                                dq)
+    torch.cuda.synchronize()
+    dq_ref = np.zeros((sq, hq, d))
+    for i, (n, m) in enumerate(specs):
+        if n == 0:
+            continue  # an empty chunk adds nothing
+        a, bk, bv = oracle.chunk_backward(q.cpu(), ks[i].cpu(), vs[i].cpu(), d_o.cpu(), o32, l32, qp, _pos(m, n),
+                                          causal=True)
+        dq_ref += a
+        compare_grad(dks[i].cpu().numpy(), bk, TOL_GRAD_BF16, f"64-chunk dK {i}")
+        compare_grad(dvs[i].cpu().numpy(), bv, TOL_GRAD_BF16, f"64-chunk dV {i}")
+    compare_grad(dq.cpu().numpy(), dq_ref, TOL_GRAD_BF16, "64-chunk dQ")
