@@ -291,3 +291,28 @@ def test_chunk_lists_at_the_maximum():
         compare_grad(dks[i].cpu().numpy(), bk, TOL_GRAD_BF16, f"64-chunk dK {i}")
         compare_grad(dvs[i].cpu().numpy(), bv, TOL_GRAD_BF16, f"64-chunk dV {i}")
     compare_grad(dq.cpu().numpy(), dq_ref, TOL_GRAD_BF16, "64-chunk dQ")
+
+
+def test_empty_query_shard_everywhere():
+    """A rank with no query rows (sq = 0): every call succeeds, launches nothing harmful and
+    leaves the other operands untouched -- partial, chunk list, merge, backward prep, backward of
+    one chunk and of a chunk list (whose dK, dV must stay as they were)."""
+    hq, hkv, d = 4, 2, 128
+    q = torch.empty((0, hq, d), dtype=torch.bfloat16, device=DEV)
+    k = wl.normal((200, hkv, d), torch.bfloat16, 81, 0.5, device=DEV)
+    v = wl.normal((200, hkv, d), torch.bfloat16, 82, 1.0, device=DEV)
+    qm, km = PosMap(0, 1), PosMap(0, 1)
+    o, lse = cpa.partial_attn(q, k, v, qm, km, causal=True)
+    assert o.shape == (0, hq, d) and lse.shape == (0, hq)
+    o2, l2 = cpa.partial_attn_chunks(q, [(k, v, km), (k, v, PosMap(500, 1))], qm, causal=True)
+    assert o2.shape == (0, hq, d)
+    om, lm = cpa.merge_partials([o, o], [lse, lse])
+    assert om.shape == (0, hq, d)
+    aux = cpa.attn_bwd_prep(o, q, lse)
+    dq = torch.zeros((0, hq, d), device=DEV)
+    dk = torch.full(k.shape, 0.5, device=DEV)
+    dv = torch.full(v.shape, 0.5, device=DEV)
+    cpa.partial_attn_bwd(q, k, v, q, aux, qm, km, dq, dk, dv, causal=True)
+    cpa.partial_attn_bwd_chunks(q, q, aux, qm, [(k, v, km, dk, dv)], dq)
+    torch.cuda.synchronize()
+    assert torch.all(dk == 0.5) and torch.all(dv == 0.5)
