@@ -316,3 +316,36 @@ def test_empty_query_shard_everywhere():
     cpa.partial_attn_bwd_chunks(q, q, aux, qm, [(k, v, km, dk, dv)], dq)
     torch.cuda.synchronize()
     assert torch.all(dk == 0.5) and torch.all(dv == 0.5)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_large_logits(d):
+    """Scores with a spread of tens (q, k ~ N(0, 6^2)): the running maximum jumps often, so the
+    lazy rescale of O and l runs many times, and most probabilities underflow -- the result must
+    still match the oracle (forward per chunk and over a chunk list, and the backward)."""
+    sq, hq, hkv = 300, 4, 2
+    qm, km1, km2 = PosMap(300, 1), PosMap(0, 1), PosMap(150, 2)
+    q = wl.normal((sq, hq, d), torch.bfloat16, 91, 6.0, device=DEV)
+    k1 = wl.normal((400, hkv, d), torch.bfloat16, 92, 6.0, device=DEV)
+    v1 = wl.normal((400, hkv, d), torch.bfloat16, 93, 1.0, device=DEV)
+    k2 = wl.normal((200, hkv, d), torch.bfloat16, 94, 6.0, device=DEV)
+    v2 = wl.normal((200, hkv, d), torch.bfloat16, 95, 1.0, device=DEV)
+    d_o = wl.normal((sq, hq, d), torch.bfloat16, 96, 1.0, device=DEV)
+    qp, kp1, kp2 = _pos(qm, sq), _pos(km1, 400), _pos(km2, 200)
+    o, lse = cpa.partial_attn(q, k1, v1, qm, km1, causal=True)
+    ro, rl = oracle.attention(q.cpu(), k1.cpu(), v1.cpu(), qp, kp1, causal=True)
+    compare_partial(o.cpu().numpy(), lse.cpu().numpy(), ro, rl, TOL_BF16_O, TOL_BF16_LSE, f"large logits d={d}")
+    o2, l2 = cpa.partial_attn_chunks(q, [(k2, v2, km2), (k1, v1, km1)], qm, causal=True)
+    ro2, rl2 = oracle.attention(q.cpu(), torch.cat([k1.cpu(), k2.cpu()]), torch.cat([v1.cpu(), v2.cpu()]), qp,
+                                np.concatenate([kp1, kp2]), causal=True)
+    compare_partial(o2.cpu().numpy(), l2.cpu().numpy(), ro2, rl2, TOL_BF16_O, TOL_BF16_LSE, f"large logits chunks d={d}")
+    o32, l32 = torch.from_numpy(ro2).float(), torch.from_numpy(rl2).float()
+    aux = cpa.attn_bwd_prep(o32.to(DEV), d_o, l32.to(DEV))
+    dq = torch.zeros(q.shape, device=DEV)
+    dk = torch.zeros(k1.shape, device=DEV)
+    dv = torch.zeros(v1.shape, device=DEV)
+    cpa.partial_attn_bwd(q, k1, v1, d_o, aux, qm, km1, dq, dk, dv, causal=True)
+    torch.cuda.synchronize()
+    ref = oracle.chunk_backward(q.cpu(), k1.cpu(), v1.cpu(), d_o.cpu(), o32, l32, qp, kp1, causal=True)
+    for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        compare_grad(g.cpu().numpy(), r, TOL_GRAD_BF16, f"large logits {name} d={d}")
