@@ -103,3 +103,14 @@ def test_noalloc_rejects_oversize_on_gpu():
     dk = torch.zeros(k.shape, dtype=torch.float32, device=dev)
     with pytest.raises(cpa.CpError, match="limit"):
         cpa.partial_attn_bwd_noalloc(q, k, k, q, q, lse, PosMap(0, 1), PosMap(0, 1), dq, dk, dk.clone())
+
+
+def test_noalloc_binding_rejects_bad_tensors():
+    """The Python binding checks devices and shapes before calling the library (no GPU needed)."""
+    q = torch.zeros((4, 2, 64), dtype=torch.bfloat16)
+    k = torch.zeros((4, 1, 64), dtype=torch.bfloat16)
+    lse = torch.zeros((4, 2))
+    g = torch.zeros((4, 2, 64))
+    gk = torch.zeros((4, 1, 64))
+    with pytest.raises(cpa.CpError):  # host tensors
+        cpa.partial_attn_bwd_noalloc(q, k, k, q, q, lse, PosMap(0, 1), PosMap(0, 1), g, gk, gk.clone())
