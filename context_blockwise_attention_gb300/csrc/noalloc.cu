@@ -17,13 +17,13 @@
 
 #include "internal.h"
 
+// The shared workspace.  Every call overwrites all of the part it uses (prep writes every row,
+// padding rows included, before the backward reads any), so nothing has to start at zero.
+static __device__ __align__(256) float g_noalloc_aux[CP_NOALLOC_AUX_MAX_FLOATS];
+
 namespace {
 
 constexpr int kMaxDev = 64;
-
-// The shared workspace.  Every call overwrites all of the part it uses (prep writes every row,
-// padding rows included, before the backward reads any), so nothing has to start at zero.
-__device__ __align__(256) float g_noalloc_aux[CP_NOALLOC_AUX_MAX_FLOATS];
 
 std::mutex g_mu;
 float* g_aux_addr[kMaxDev];  // device address of g_noalloc_aux, per device, once looked up
