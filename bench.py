@@ -5,8 +5,11 @@ the device), a partial attention per KV chunk in the seeded arrival order, and t
 partials (workloads 1, 2, 3, 5); or, for the Ulysses workload 4, the seq->head reshard of Q and
 of fused K|V, full-sequence attention per head-rank and the head->seq reshard of O.
 
-Default workload (N=1): 2 -- causal bf16 GQA 32/8, D=128, S=32768, CP=8 strided, rank 7's 4096
-queries against the 8 KV chunks in a seeded random order.
+Default run (N=1): the headline is workload 5 -- the largest single-GPU workload by sequence:
+causal bf16 GQA 64/8, D=64, S=262144, CP=8 strided, rank 7's 32768 queries against 64 KV chunks
+of 4096 tokens in a seeded random order, K with outliers.  The same line carries a ``configs``
+object with every workload (1, 2, 3 under both the strided and the contiguous layout, 4, 5),
+each timed on its own with its own clock record.  ``--config N`` times one workload alone.
 
 Prints one JSON line.  ``value`` is causal-adjusted attention TFLOP/s over the device-timed
 step (FLOPs = 4 * D * Hq * exact visible (q, k) pairs); ``e2e`` is the same metric through the
@@ -38,6 +41,30 @@ sys.path.insert(0, ROOT)
 
 METRIC = "causal-adjusted attention TFLOP/s and % bf16 roofline; merge/reshard HBM GB/s"
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB of L2
+
+
+# ----------------------------------------------------------------------------- FLOP accounting
+
+def visible_pairs(q_map, n_q, k_map, n_k, causal=True):
+    """Exact count of (query, key) pairs with kv_pos <= q_pos between an affine query block and
+    an affine KV chunk (the causal-adjusted FLOP count's N_vis).  Accounting only: no kernel or
+    test result depends on it."""
+    if not causal:
+        return int(n_q) * int(n_k)
+    qp = q_map.base + q_map.stride * np.arange(n_q, dtype=np.int64)
+    cnt = np.where(qp < k_map.base, 0, (qp - k_map.base) // k_map.stride + 1)
+    return int(np.minimum(cnt, n_k).sum())
+
+
+def finite_rows(q_map, n_q, k_map, n_k, causal=True):
+    """Query rows that see at least one key of the chunk (rows whose partial LSE is finite): the
+    merge reads O only for those (its algorithmic byte count)."""
+    if n_k == 0:
+        return 0
+    if not causal:
+        return int(n_q)
+    qp = q_map.base + q_map.stride * np.arange(n_q, dtype=np.int64)
+    return int((qp >= k_map.base).sum())
 
 
 def _peaks():
@@ -153,7 +180,7 @@ class Step:
                 o_parts, l_parts, seg_calls, seg_chunks = [], [], [], []
                 for ci in order:
                     src, lo, nk, kmap = plan[int(ci)]
-                    n_vis = cpa.visible_pairs(qmap, nq, kmap, nk, w.causal)
+                    n_vis = visible_pairs(qmap, nq, kmap, nk, w.causal)
                     if w.causal and n_vis == 0:
                         continue  # chunk entirely in the future of this query block: never issued
                     k, v = kv[src]
@@ -166,7 +193,7 @@ class Step:
                     self.flops += 4 * w.d * w.hq * n_vis
                     o_parts.append(o)
                     l_parts.append(l)
-                    fr = cpa.finite_rows(qmap, nq, kmap, nk, w.causal)
+                    fr = finite_rows(qmap, nq, kmap, nk, w.causal)
                     self.merge_bytes += nq * w.hq * 4 + fr * w.hq * w.d * 4
                 o_seg, l_seg = out[row:row + nq], lse[row:row + nq]
                 self.blocks.append((qr, qs, o_seg, l_seg, qmap, seg_chunks))
@@ -203,7 +230,7 @@ class Step:
                    for _ in range(cp)]
         self._output_tensors = self.xo
         full = cpa.PosMap(0, 1)
-        n_vis = cpa.visible_pairs(full, S, full, S, True)
+        n_vis = visible_pairs(full, S, full, S, True)
         for r in range(cp):
             self.attn_calls.append(dict(q=self.yq[r], k=self.yk[r], v=self.yv[r], q_pos=full,
                                         kv_pos=full, causal=True, o=self.yo[r], lse=self.ylse[r]))
@@ -369,7 +396,7 @@ class BwdStep:
                 k, v = fwd.kv[src]
                 clist.append((k[lo:lo + nk], v[lo:lo + nk], kmap, self.dk[src][lo:lo + nk], self.dv[src][lo:lo + nk]))
                 # five products of 2*D flops per visible pair: S, dP, dV, dK, dQ
-                self.flops += 10 * w.d * w.hq * cpa.visible_pairs(qmap, nq, kmap, nk, w.causal)
+                self.flops += 10 * w.d * w.hq * visible_pairs(qmap, nq, kmap, nk, w.causal)
             if fused:
                 # the block's whole chunk list in one call (one launch per 32 chunks)
                 self.calls.append((cpa.partial_attn_bwd_chunks,
@@ -430,7 +457,7 @@ class UlyssesBwdStep:
         self.dks = [torch.empty((S // cp, w.hkv, w.d), device=dev) for _ in range(cp)]
         self.dvs = [torch.empty((S // cp, w.hkv, w.d), device=dev) for _ in range(cp)]
         full = cpa.PosMap(0, 1)
-        self.flops = cp * 10 * w.d * hl * cpa.visible_pairs(full, S, full, S, True)
+        self.flops = cp * 10 * w.d * hl * visible_pairs(full, S, full, S, True)
         # reshard bytes: dO (bf16) in, dQ and dK|dV (fp32) out; one read and one write each
         self.reshard_bytes = 2 * S * w.d * (w.hq * 2 + (w.hq + 2 * w.hkv) * 4)
 
@@ -653,17 +680,18 @@ def _config_dict(w, layout, extra):
 def run_reference(args):
     world, rank, _ = _dist()
     from context_blockwise_attention_gb300 import workloads as wl
-    w = wl.WORKLOADS[args.config]
+    cfg = args.config or HEADLINE_CONFIG
+    w = wl.WORKLOADS[cfg]
     if world > 1 and rank != 0:
         return
     # bounded: about 64 x 10 sampled rows over the whole timed run, whatever --steps is
     rows = args.ref_rows or max(4, (64 * 10) // max(1, args.steps))
     for _ in range(args.warmup):
-        oracle_sample(args.config, max(1, rows // 4), layout=args.layout)
+        oracle_sample(cfg, max(1, rows // 4), layout=args.layout)
     times, fl = [], 0
     desc = ""
     for _ in range(args.steps):
-        t, fl, desc = oracle_sample(args.config, rows, layout=args.layout)
+        t, fl, desc = oracle_sample(cfg, rows, layout=args.layout)
         times.append(t)
     tmean = sum(times) / len(times)
     value = fl / tmean / 1e12
@@ -680,6 +708,206 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def _timed_steps(fn, steps, stream, flush):
+    """`steps` calls of fn, each preceded by an L2 flush and bracketed by CUDA events on the
+    launching stream with a synchronize after; returns (per-step ms, summed return values)."""
+    ms, total = [], 0
+    for _ in range(steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        total += fn() or 0
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    return ms, total
+
+
+def measure(cfg, layout, dev, world, local, steps, warmup, flush, *, fused_path=False, full=True,
+            fused_extra=True, backward_extra=True):
+    """Time one workload: the device-resident step (attention, merge / reshard segments), and,
+    with ``full``, the end-to-end step through host buffers; the fused chunk-list path (f1) and
+    the backward (f4) ride along unless switched off.  Returns (summary dict, step)."""
+    from context_blockwise_attention_gb300 import workloads as wl
+    w = wl.WORKLOADS[cfg]
+    qr = None
+    if w.query_rank >= 0:
+        _, rank, _ = _dist()
+        qr = (w.cp - 1 - rank) % w.cp
+    stream = torch.cuda.current_stream()
+    peaks = _peaks()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    step = Step(cfg, dev, query_rank=qr, layout=layout, host_copy=full, fused=fused_path)
+    for _ in range(warmup):
+        step.run()
+    barrier()
+
+    # ---- device-timed steps (inputs resident), L2 flushed before each
+    timers = {"attn": [], "merge": [], "reshard": []}
+    if len(step.rank_plans) > 1:
+        timers["rank_attn"] = []
+    sampler = ClockSampler(local)
+    sampler.start()
+    step_ms, launches = _timed_steps(lambda: step.run(timers), steps, stream, flush)
+    barrier()
+    clocks = sampler.stop()
+    ms_per_step, value = aggregate(sum(step_ms), step.flops, steps, world, dev)
+
+    def seg(name):
+        # total device time of one kind of launch per step (a step may record several intervals)
+        xs = [s.elapsed_time(e) for s, e in timers[name]]
+        return sum(xs) / steps if xs else None
+    attn_ms, merge_ms, reshard_ms = seg("attn"), seg("merge"), seg("reshard")
+    achieved = step.flops / (attn_ms * 1e-3) / 1e12
+    if w.dtype == "f32":
+        # fp32 inputs run on CUDA cores (FFMA): the peak is SMs x 128 FMA lanes x 2 flops x the
+        # maximum SM clock (no measured FFMA peak is available)
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        mhz = clocks.get("sm_max_mhz") or 2070.0
+        peak = sms * 128 * 2 * mhz * 1e6 / 1e12
+        roofline = {"bound": "alu", "kernel": "attn_simt_kernel", "achieved": achieved, "peak": peak,
+                    "unit": "TFLOP/s", "frac": achieved / peak,
+                    "peak_source": f"derived: {sms} SMs x 128 FFMA/clk x 2 x {mhz:.0f} MHz",
+                    "launches_per_step": len(step.attn_calls) + len(step.fused_calls), "traffic": None}
+    else:
+        traffic = _profile_traffic(os.path.join(ROOT, "context_blockwise_attention_gb300", "csrc", "attn_tc.cu"),
+                                   f"cfg{cfg}" + ("_fused" if step.fused else ""))
+        roofline = {"bound": "tensor", "kernel": "attn_tc_kernel", "achieved": achieved,
+                    "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16"],
+                    "peak_source": f"{peaks['source']} bf16 dense (burst)",
+                    "frac_of_sustained": achieved / peaks["bf16_sustained"],
+                    "launches_per_step": len(step.attn_calls) + len(step.fused_calls),
+                    "traffic": traffic}
+    out = {"workload": f"cfg{cfg}: {w.name}", "layout": layout, "steps": steps, "warmup": warmup,
+           "value": value, "unit": "TFLOP/s", "ms_per_step": ms_per_step,
+           "ms_median": float(np.median(step_ms)), "ms_best": float(min(step_ms)),
+           "path": "fused chunk list" if step.fused else ("Ulysses reshards + full-sequence attention"
+                                                          if cfg == 4 else "partial per chunk + merge"),
+           "gpu_launches": launches, "attn_ms_per_step": attn_ms, "attn_tflops": achieved,
+           "attn_frac": roofline["frac"], "step_flop": step.flops, "query_rank": qr,
+           "roofline": roofline, "clocks": clocks}
+    if timers.get("rank_attn"):
+        # every simulated rank's attention time: with one GPU per rank the step would wait for
+        # the slowest, so max / mean shows the layout's load balance
+        per = {}
+        for r_, s_, e_ in timers["rank_attn"]:
+            per[r_] = per.get(r_, 0.0) + s_.elapsed_time(e_) / steps
+        ms = [per[r_] for r_ in sorted(per)]
+        out["per_rank_attn_ms"] = ms
+        out["simulated_parallel_attn_ms"] = max(ms)
+        out["rank_balance_max_over_mean"] = max(ms) / (sum(ms) / len(ms))
+    if merge_ms:
+        gbs = step.merge_bytes / (merge_ms * 1e-3) / 1e9
+        out["merge"] = {"ms": merge_ms, "GB/s": gbs, "frac": gbs / peaks["hbm"], "bytes": step.merge_bytes,
+                        "peak": peaks["hbm"], "bound": "hbm"}
+    if reshard_ms:
+        gbs = step.reshard_bytes / (reshard_ms * 1e-3) / 1e9
+        out["reshard"] = {"ms": reshard_ms, "GB/s": gbs, "frac": gbs / peaks["hbm"], "bytes": step.reshard_bytes,
+                          "peak": peaks["hbm"], "bound": "hbm"}
+
+    if full:
+        # ---- end to end through the C ABI with host buffers
+        for _ in range(2):
+            step.run_e2e()
+        barrier()
+        e2e_ms, _ = _timed_steps(step.run_e2e, steps, stream, flush)
+        e2e_ms_per_step, e2e_value = aggregate(sum(e2e_ms), step.flops, steps, world, dev)
+        out["e2e"] = {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": step.h2d_bytes,
+                      "d2h_bytes_per_step": step.d2h_bytes, "ms_per_step": e2e_ms_per_step}
+
+    if fused_extra and not step.fused and cfg != 4:
+        # the same workload through the fused chunk-list path (f1), timed the same way
+        fstep = Step(cfg, dev, query_rank=qr, layout=layout, fused=True)
+        for _ in range(warmup):
+            fstep.run()
+        barrier()
+        fattn = {"attn": [], "merge": [], "reshard": []}
+        sampler = ClockSampler(local)
+        sampler.start()
+        fms, _ = _timed_steps(lambda: fstep.run(fattn), steps, stream, flush)
+        barrier()
+        fclocks = sampler.stop()
+        f_ms, f_value = aggregate(sum(fms), fstep.flops, steps, world, dev)
+        f_attn_ms = sum(s_.elapsed_time(e_) for s_, e_ in fattn["attn"]) / steps
+        f_ach = fstep.flops / (f_attn_ms * 1e-3) / 1e12
+        out["fused"] = {"value": f_value, "unit": "TFLOP/s", "ms_per_step": f_ms,
+                        "attn_tflops": f_ach, "attn_frac": f_ach / roofline["peak"],
+                        "launches_per_step": len(fstep.fused_calls), "clocks": fclocks,
+                        "path": "one cp_partial_attn_chunks per query block (no partials, no merge)"}
+        del fstep
+    if backward_extra:
+        # the backward of the same workload (f4), timed the same way (L2 flushed per step)
+        if cfg == 4:
+            bstep = UlyssesBwdStep(Step(4, dev))
+        else:
+            bstep = BwdStep(Step(cfg, dev, query_rank=qr, layout=layout, fused=True))
+        for _ in range(warmup):
+            bstep.run()
+        barrier()
+        btimes, rtimes = [], []
+        sampler = ClockSampler(local)
+        sampler.start()
+        bms, blaunch = _timed_steps((lambda: bstep.run(btimes, rtimes)) if cfg == 4 else
+                                    (lambda: bstep.run(btimes)), steps, stream, flush)
+        barrier()
+        bclocks = sampler.stop()
+        b_ms, b_value = aggregate(sum(bms), bstep.flops, steps, world, dev)
+        b_kernel_ms = sum(s_.elapsed_time(e_) for s_, e_ in btimes) / steps
+        b_ach = bstep.flops / (b_kernel_ms * 1e-3) / 1e12
+        out["backward"] = {
+            "value": b_value, "unit": "TFLOP/s", "ms_per_step": b_ms,
+            "step_flop": bstep.flops, "flop_per_visible_pair": 10 * w.d * w.hq,
+            "kernel": "attn_bwd_tc_kernel" if w.dtype == "bf16" else "bwd_simt_dkdv_kernel + bwd_simt_dq_kernel",
+            "kernel_ms_per_step": b_kernel_ms, "achieved": b_ach,
+            "peak": roofline["peak"], "frac": b_ach / roofline["peak"], "bound": roofline["bound"],
+            "launches_per_step": blaunch // steps, "clocks": bclocks,
+            "path": ("dO seq->head, per head-rank prep + full-sequence cp_partial_attn_bwd, "
+                     "dQ and dK|dV head->seq (fp32); gradients zeroed in the step")
+            if cfg == 4 else
+            ("prep per query block + one cp_partial_attn_bwd_chunks per block over its chunk list; "
+             "dK/dV accumulated into the chunk owners' shards; gradients zeroed in the step")}
+        if rtimes:
+            r_ms = sum(s_.elapsed_time(e_) for s_, e_ in rtimes) / steps
+            gbs = bstep.reshard_bytes / (r_ms * 1e-3) / 1e9
+            out["backward"]["reshard"] = {"ms": r_ms, "GB/s": gbs, "frac": gbs / peaks["hbm"],
+                                          "bytes": bstep.reshard_bytes}
+        del bstep
+    return out, step
+
+
+# every workload of the default line: (key, workload, layout); workload 3 under both layouts it
+# is specified with
+ALL_CONFIGS = [("cfg1", 1, "contiguous"), ("cfg2", 2, "strided"), ("cfg3_strided", 3, "strided"),
+               ("cfg3_contiguous", 3, "contiguous"), ("cfg4", 4, "contiguous"), ("cfg5", 5, "strided")]
+HEADLINE_CONFIG = 5
+
+
+def cpu_baseline(cfg, layout, ref_rows, step_flops):
+    """The oracle as it stands, timed on this host's cores on a bounded sample (about 10 s)."""
+    from context_blockwise_attention_gb300 import workloads as wl
+    w = wl.WORKLOADS[cfg]
+    if ref_rows:
+        t, fl, desc = oracle_sample(cfg, ref_rows, layout=layout)
+    else:
+        # about 10 s of oracle work: time 16 rows, then size the sample from that rate
+        t16, _, _ = oracle_sample(cfg, 16, layout=layout)
+        rows = int(min(max(16, 16 * 10.0 / max(t16, 1e-3)), w.local_len if cfg != 4 else w.seq_len))
+        t, fl, desc = oracle_sample(cfg, rows, layout=layout)
+    return {"value": fl / t / 1e12, "unit": "TFLOP/s", "cores": _blas_threads(),
+            "kind": "oracle", "sample": desc, "seconds": t,
+            # 4*D*Hq flops per visible pair: the sample's rate in pairs/s, and the whole
+            # workload's time at that rate (extrapolated, not measured)
+            "pairs_per_s": fl / (4 * w.d * (w.hq // (w.cp if cfg == 4 else 1))) / t,
+            "extrapolated_full_workload_s": step_flops / (fl / t)}
+
+
 def run_gpu(args):
     world, rank, local = _dist()
     torch.cuda.set_device(local)
@@ -690,345 +918,254 @@ def run_gpu(args):
     import context_blockwise_attention_gb300 as cpa
     from context_blockwise_attention_gb300 import workloads as wl
     cpa.load_library()
-    w = wl.WORKLOADS[args.config]
+    all_configs = args.config is None
+    cfg = HEADLINE_CONFIG if all_configs else args.config
+    w = wl.WORKLOADS[cfg]
     layout = args.layout or w.layout
-    qr = None
-    if w.query_rank >= 0:
-        qr = (w.cp - 1 - rank) % w.cp
-    step = Step(args.config, dev, query_rank=qr, layout=layout, host_copy=True, fused=args.fused)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    def barrier():
-        torch.cuda.synchronize()
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
+    head, step = measure(cfg, layout, dev, world, local, args.steps, args.warmup, flush,
+                         fused_path=args.fused, full=True, fused_extra=not args.no_fused,
+                         backward_extra=not args.no_backward)
+    step_flops = step.flops
+    del step
+    torch.cuda.empty_cache()
 
-    for _ in range(args.warmup):
-        step.run()
-    barrier()
+    configs = None
+    if all_configs and not args.headline_only:
+        # every workload on its own, timed the same way (its own clock record); the headline's
+        # entry is the summary above
+        configs = {}
+        sub_steps = min(args.steps, args.config_steps)
+        for key, c, lay in ALL_CONFIGS:
+            if c == cfg and lay == layout:
+                res = head
+            else:
+                res, st = measure(c, lay, dev, world, local, sub_steps, args.warmup, flush, full=False,
+                                  fused_extra=not args.no_fused, backward_extra=not args.no_backward)
+                del st
+                torch.cuda.empty_cache()
+            e = {k: res[k] for k in ("workload", "layout", "steps", "value", "ms_per_step", "attn_tflops",
+                                     "attn_frac", "clocks") if k in res}
+            e["attn_bound"] = res["roofline"]["bound"]
+            e["attn_peak"] = res["roofline"]["peak"]
+            for k in ("merge", "reshard"):
+                if k in res:
+                    e[k] = {x: res[k][x] for x in ("GB/s", "frac", "ms", "bytes")}
+            if "fused" in res:
+                e["fused_attn_tflops"] = res["fused"]["attn_tflops"]
+                e["fused_attn_frac"] = res["fused"]["attn_frac"]
+            if "backward" in res:
+                e["backward_kernel_tflops"] = res["backward"]["achieved"]
+                e["backward_frac"] = res["backward"]["frac"]
+            if "rank_balance_max_over_mean" in res:
+                e["rank_balance_max_over_mean"] = res["rank_balance_max_over_mean"]
+            configs[key] = e
 
-    # ---- device-timed steps (inputs resident), L2 flushed before each
-    timers = {"attn": [], "merge": [], "reshard": []}
-    if len(step.rank_plans) > 1:
-        timers["rank_attn"] = []
-    sampler = ClockSampler(local)
-    sampler.start()
-    step_ms, launches = [], 0
-    stream = torch.cuda.current_stream()
-    for _ in range(args.steps):
-        flush.zero_()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        launches += step.run(timers)
-        b.record(stream)
-        torch.cuda.synchronize()
-        step_ms.append(a.elapsed_time(b))
-    barrier()
-    clocks = sampler.stop()
-    ms_per_step, value = aggregate(sum(step_ms), step.flops, args.steps, world, dev)
-
-    def seg(name):
-        # total device time of one kind of launch per step (a step may record several intervals)
-        xs = [s.elapsed_time(e) for s, e in timers[name]]
-        return sum(xs) / args.steps if xs else None
-    attn_ms = seg("attn")
-    merge_ms = seg("merge")
-    reshard_ms = seg("reshard")
-
-    # ---- end to end through the C ABI with host buffers
-    for _ in range(2):
-        step.run_e2e()
-    barrier()
-    e2e_ms = []
-    for _ in range(args.steps):
-        flush.zero_()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        step.run_e2e()
-        b.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms.append(a.elapsed_time(b))
-    e2e_ms_per_step, e2e_value = aggregate(sum(e2e_ms), step.flops, args.steps, world, dev)
-
-    peaks = _peaks()
-    n_attn = len(step.attn_calls) + len(step.fused_calls)
-    achieved = step.flops / (attn_ms * 1e-3) / 1e12
-    traffic = _profile_traffic(os.path.join(ROOT, "context_blockwise_attention_gb300", "csrc",
-                                            "attn_tc.cu"), f"cfg{args.config}")
-    if w.dtype == "f32":
-        # fp32 inputs run on CUDA cores (FFMA): the peak is SMs x 128 FMA lanes x 2 flops x the
-        # maximum SM clock (no measured FFMA peak is available)
-        sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        mhz = clocks.get("sm_max_mhz") or 2070.0
-        ffma_peak = sms * 128 * 2 * mhz * 1e6 / 1e12
-        roofline = {"bound": "alu", "kernel": "attn_simt_kernel", "achieved": achieved, "peak": ffma_peak,
-                    "unit": "TFLOP/s", "frac": achieved / ffma_peak,
-                    "peak_source": f"derived: {sms} SMs x 128 FFMA/clk x 2 x {mhz:.0f} MHz",
-                    "launches_per_step": n_attn, "traffic": None}
-    else:
-        roofline = {"bound": "tensor", "kernel": "attn_tc_kernel", "achieved": achieved,
-                    "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16"],
-                    "peak_source": f"{peaks['source']} bf16 dense (burst)",
-                    "frac_of_sustained": achieved / peaks["bf16_sustained"],
-                    "launches_per_step": n_attn,
-                    "traffic": traffic}
-    extra = {"attn_ms_per_step": attn_ms, "attn_tflops": achieved,
-             "step_flop": step.flops, "query_rank": qr}
-    if timers.get("rank_attn"):
-        # every simulated rank's attention time: with one GPU per rank the step would wait for
-        # the slowest, so max / mean shows the layout's load balance
-        per = {}
-        for r_, s_, e_ in timers["rank_attn"]:
-            per[r_] = per.get(r_, 0.0) + s_.elapsed_time(e_) / args.steps
-        ms = [per[r_] for r_ in sorted(per)]
-        extra["per_rank_attn_ms"] = ms
-        extra["simulated_parallel_attn_ms"] = max(ms)
-        extra["rank_balance_max_over_mean"] = max(ms) / (sum(ms) / len(ms))
-    if merge_ms:
-        gbs = step.merge_bytes / (merge_ms * 1e-3) / 1e9
-        extra["merge"] = {"ms": merge_ms, "GB/s": gbs, "frac": gbs / peaks["hbm"],
-                          "bytes": step.merge_bytes}
-    if reshard_ms:
-        gbs = step.reshard_bytes / (reshard_ms * 1e-3) / 1e9
-        extra["reshard"] = {"ms": reshard_ms, "GB/s": gbs, "frac": gbs / peaks["hbm"],
-                            "bytes": step.reshard_bytes}
-
-    fused = None
-    if not args.fused and args.config != 4 and not args.no_fused:
-        # the same workload through the fused chunk-list path (f1), timed the same way
-        fstep = Step(args.config, dev, query_rank=qr, layout=layout, fused=True)
-        for _ in range(args.warmup):
-            fstep.run()
-        barrier()
-        fms, fattn = [], {"attn": [], "merge": [], "reshard": []}
-        for _ in range(args.steps):
-            flush.zero_()
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fstep.run(fattn)
-            b.record(stream)
-            torch.cuda.synchronize()
-            fms.append(a.elapsed_time(b))
-        barrier()
-        f_ms, f_value = aggregate(sum(fms), fstep.flops, args.steps, world, dev)
-        f_attn_ms = sum(s_.elapsed_time(e_) for s_, e_ in fattn["attn"]) / args.steps
-        f_ach = fstep.flops / (f_attn_ms * 1e-3) / 1e12
-        fused = {"value": f_value, "unit": "TFLOP/s", "ms_per_step": f_ms,
-                 "attn_tflops": f_ach, "attn_frac": f_ach / peaks["bf16"],
-                 "launches_per_step": len(fstep.fused_calls),
-                 "path": "one cp_partial_attn_chunks per query block (no partials, no merge)"}
-        del fstep
-    backward = None
-    if not args.no_backward:
-        # the backward of the same workload (f4), timed the same way (L2 flushed per step)
-        if args.config == 4:
-            bstep = UlyssesBwdStep(Step(4, dev))
-        else:
-            bstep = BwdStep(Step(args.config, dev, query_rank=qr, layout=layout, fused=True))
-        for _ in range(args.warmup):
-            bstep.run()
-        barrier()
-        bms, btimes, rtimes, blaunch = [], [], [], 0
-        for _ in range(args.steps):
-            flush.zero_()
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            blaunch += bstep.run(btimes, rtimes) if args.config == 4 else bstep.run(btimes)
-            b.record(stream)
-            torch.cuda.synchronize()
-            bms.append(a.elapsed_time(b))
-        barrier()
-        b_ms, b_value = aggregate(sum(bms), bstep.flops, args.steps, world, dev)
-        b_kernel_ms = sum(s_.elapsed_time(e_) for s_, e_ in btimes) / args.steps
-        b_ach = bstep.flops / (b_kernel_ms * 1e-3) / 1e12
-        backward = {"value": b_value, "unit": "TFLOP/s", "ms_per_step": b_ms,
-                    "step_flop": bstep.flops, "flop_per_visible_pair": 10 * w.d * w.hq,
-                    "kernel": "attn_bwd_tc_kernel" if w.dtype == "bf16" else "bwd_simt_dkdv_kernel + bwd_simt_dq_kernel",
-                    "kernel_ms_per_step": b_kernel_ms, "achieved": b_ach,
-                    "peak": roofline["peak"], "frac": b_ach / roofline["peak"], "bound": roofline["bound"],
-                    "launches_per_step": blaunch // args.steps,
-                    "path": ("dO seq->head, per head-rank prep + full-sequence cp_partial_attn_bwd, "
-                             "dQ and dK|dV head->seq (fp32); gradients zeroed in the step")
-                    if args.config == 4 else
-                    ("prep per query block + one cp_partial_attn_bwd_chunks per block over its chunk list; "
-                     "dK/dV accumulated into the chunk owners' shards; gradients zeroed in the step")}
-        if rtimes:
-            r_ms = sum(s_.elapsed_time(e_) for s_, e_ in rtimes) / args.steps
-            gbs = bstep.reshard_bytes / (r_ms * 1e-3) / 1e9
-            backward["reshard"] = {"ms": r_ms, "GB/s": gbs, "frac": gbs / peaks["hbm"], "bytes": bstep.reshard_bytes}
-        del bstep
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        if args.ref_rows:
-            t, fl, desc = oracle_sample(args.config, args.ref_rows, layout=layout)
-        else:
-            # about 10 s of oracle work: time 16 rows, then size the sample from that rate
-            t16, _, _ = oracle_sample(args.config, 16, layout=layout)
-            rows = int(min(max(16, 16 * 10.0 / max(t16, 1e-3)), w.local_len if args.config != 4 else w.seq_len))
-            t, fl, desc = oracle_sample(args.config, rows, layout=layout)
-        cpu = {"value": fl / t / 1e12, "unit": "TFLOP/s", "cores": _blas_threads(),
-               "kind": "oracle", "sample": desc, "seconds": t,
-               # 4*D*Hq flops per visible pair: the sample's rate in pairs/s, and the whole
-               # workload's time at that rate (extrapolated, not measured)
-               "pairs_per_s": fl / (4 * w.d * (w.hq // (w.cp if args.config == 4 else 1))) / t,
-               "extrapolated_full_workload_s": step.flops / (fl / t)}
+        cpu = cpu_baseline(cfg, layout, args.ref_rows, step_flops)
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-                "ms_median": float(np.median(step_ms)), "ms_best": float(min(step_ms)),
+        cfg_extra = {"parallelism": f"replicas x{world}", "path": head["path"]}
+        line = {"metric": METRIC, "value": head["value"], "unit": "TFLOP/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+                "ms_median": head["ms_median"], "ms_best": head["ms_best"],
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16" if w.dtype == "bf16" else "f32",
                 "data": "synthetic (seeded N(0,1) inputs; no dataset or weights)",
-                "config": _config_dict(w, layout, {"parallelism": f"replicas x{world}",
-                                                   "path": "fused chunk list" if step.fused
-                                                   else "partial per chunk + merge"}),
-                "e2e": {"value": e2e_value, "unit": "TFLOP/s",
-                        "h2d_bytes_per_step": step.h2d_bytes,
-                        "d2h_bytes_per_step": step.d2h_bytes,
-                        "ms_per_step": e2e_ms_per_step},
-                "gpu_launches": launches,
-                "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks, "fused": fused,
-                "backward": backward, **extra}
+                "config": _config_dict(w, layout, cfg_extra),
+                "e2e": head["e2e"], "gpu_launches": head["gpu_launches"],
+                "roofline": head["roofline"], "cpu_baseline": cpu, "clocks": head["clocks"],
+                "fused": head.get("fused"), "backward": head.get("backward")}
+        for k in ("attn_ms_per_step", "attn_tflops", "step_flop", "query_rank", "merge", "reshard",
+                  "per_rank_attn_ms", "simulated_parallel_attn_ms", "rank_balance_max_over_mean"):
+            if k in head:
+                line[k] = head[k]
+        if configs is not None:
+            line["configs"] = configs
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
 
 
-def run_pipelined(args):
-    """Chunk arrival overlapped with compute (the FCP article, section 4.3: computation and
-    communication on different streams synchronised by CUDA events; chunks of about 4K-8K
-    tokens; too-fine chunks lose to per-chunk overhead).
+class PipelinedStep:
+    """One query rank's per-chunk path with the KV chunks arriving by copies on a second stream
+    (the FCP article, section 4.3: computation and communication on different streams,
+    synchronised by CUDA events; chunks of about 4K-8K tokens).
 
-    Each KV chunk "arrives" by a copy from pinned host memory (standing in for a slow link) on a
-    copy stream, in the seeded arrival order; the compute stream waits on that chunk's event and
-    launches its partial; the merge follows the last partial.  Compared with the serial schedule
-    (every copy, then every partial) for several chunk sizes, with the chunks coming from pinned
-    host memory and, as a fast-link case, from another device buffer.  Workload 2 (rank 7)."""
-    import context_blockwise_attention_gb300 as cpa
-    from context_blockwise_attention_gb300 import workloads as wl
+    Every source rank's shard is cut into chunks of ``chunk_tokens``; each chunk "arrives" by a
+    copy from ``source`` ("pinned_host": pinned host memory standing in for a slow link, or
+    "device": another device buffer) in the seeded arrival order.  Schedules: ``serial`` (every
+    copy, then every partial), ``overlapped`` (a receive buffer per chunk; each partial waits on
+    its own chunk's event), ``double_buffered`` (two receive buffers; the copy of chunk i waits
+    for the partial of chunk i-2); each ends with the merge.  ``merged`` is (O, LSE) of the
+    query shard."""
+
+    def __init__(self, cfg, device, chunk_tokens, source="pinned_host", query_rank=None):
+        import context_blockwise_attention_gb300 as cpa
+        from context_blockwise_attention_gb300 import workloads as wl
+        self.cpa = cpa
+        w = self.w = wl.WORKLOADS[cfg]
+        self.qr = qr = (w.query_rank if w.query_rank >= 0 else w.cp - 1) if query_rank is None else query_rank
+        self.chunk_tokens = chunk_tokens
+        self.qmap = cpa.shard_layout(w.seq_len, w.cp, qr, w.layout)
+        self.q = wl.shard_tensor(w, "q", qr, device=device)
+        host_k = [wl.shard_tensor(w, "k", r) for r in range(w.cp)]
+        host_v = [wl.shard_tensor(w, "v", r) for r in range(w.cp)]
+        if source == "pinned_host":
+            src_k, src_v = [t.pin_memory() for t in host_k], [t.pin_memory() for t in host_v]
+        else:
+            src_k, src_v = [t.to(device) for t in host_k], [t.to(device) for t in host_v]
+        self.compute, self.copy = torch.cuda.current_stream(), torch.cuda.Stream()
+        per_shard = w.local_len // chunk_tokens
+        self.n = w.cp * per_shard
+        order = wl.arrival_order(self.n, w.order_seed + 17 * qr)
+        self.chunks = []
+        self.meta = []  # (source rank, first source row, keys) per chunk, in arrival order
+        self.flops = 0
+        for ci in order:
+            src, sub = divmod(int(ci), per_shard)
+            lo, hi = sub * chunk_tokens, (sub + 1) * chunk_tokens
+            kmap = cpa.sub_chunk_map(cpa.shard_layout(w.seq_len, w.cp, src, w.layout), sub, chunk_tokens)
+            self.chunks.append(dict(
+                hk=src_k[src][lo:hi], hv=src_v[src][lo:hi], kmap=kmap,
+                dk=torch.empty((chunk_tokens, w.hkv, w.d), dtype=w.torch_dtype, device=device),
+                dv=torch.empty((chunk_tokens, w.hkv, w.d), dtype=w.torch_dtype, device=device),
+                o=torch.empty((w.local_len, w.hq, w.d), device=device),
+                l=torch.empty((w.local_len, w.hq), device=device)))
+            self.meta.append((src, lo, chunk_tokens))
+            self.flops += 4 * w.d * w.hq * visible_pairs(self.qmap, w.local_len, kmap, chunk_tokens, w.causal)
+        self.out = torch.empty((w.local_len, w.hq, w.d), dtype=w.torch_dtype, device=device)
+        self.lse = torch.empty((w.local_len, w.hq), device=device)
+        # two receive buffers for the double-buffered schedule
+        self.ring = [(torch.empty_like(self.chunks[0]["dk"]), torch.empty_like(self.chunks[0]["dv"]))
+                     for _ in range(2)]
+
+    def _partial(self, dk, dv, c):
+        self.cpa.partial_attn(self.q, dk, dv, self.qmap, c["kmap"], causal=self.w.causal, o=c["o"], lse=c["l"])
+
+    def _merge(self):
+        self.cpa.merge_partials([c["o"] for c in self.chunks], [c["l"] for c in self.chunks],
+                                o=self.out, lse=self.lse)
+
+    def _schedule(self, overlap):
+        compute, copy = self.compute, self.copy
+        evs = []
+        copy.wait_stream(compute)  # the receive buffers are free once the last step is done
+        with torch.cuda.stream(copy):
+            for c in self.chunks:
+                c["dk"].copy_(c["hk"], non_blocking=True)
+                c["dv"].copy_(c["hv"], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(copy)
+                evs.append(e)
+        if not overlap:
+            compute.wait_event(evs[-1])
+        for c, e in zip(self.chunks, evs):
+            compute.wait_event(e)
+            self._partial(c["dk"], c["dv"], c)
+        self._merge()
+
+    def serial(self):
+        self._schedule(False)
+
+    def overlapped(self):
+        self._schedule(True)
+
+    def double_buffered(self):
+        # chunk i lands in ring[i % 2]; its copy waits until the partial of chunk i - 2 has
+        # consumed that buffer (an event on the compute stream)
+        compute, copy = self.compute, self.copy
+        copy.wait_stream(compute)
+        freed = [None, None]
+        for i, c in enumerate(self.chunks):
+            dk, dv = self.ring[i % 2]
+            with torch.cuda.stream(copy):
+                if freed[i % 2] is not None:
+                    copy.wait_event(freed[i % 2])
+                dk.copy_(c["hk"], non_blocking=True)
+                dv.copy_(c["hv"], non_blocking=True)
+                arrived = torch.cuda.Event()
+                arrived.record(copy)
+            compute.wait_event(arrived)
+            self._partial(dk, dv, c)
+            done = torch.cuda.Event()
+            done.record(compute)
+            freed[i % 2] = done
+        self._merge()
+
+    def copies_only(self):
+        self.copy.wait_stream(self.compute)
+        with torch.cuda.stream(self.copy):
+            for c in self.chunks:
+                c["dk"].copy_(c["hk"], non_blocking=True)
+                c["dv"].copy_(c["hv"], non_blocking=True)
+        self.compute.wait_stream(self.copy)
+
+    def compute_only(self):
+        for c in self.chunks:
+            self._partial(c["dk"], c["dv"], c)
+        self._merge()
+
+
+def run_pipelined(args):
+    """Chunk arrival overlapped with compute (the FCP article, section 4.3), measured per chunk
+    size on workload 2 (rank 7: chunks of 512-4096 tokens) and workload 3 (rank 7: 2048-8192,
+    the page's 4K-8K range), with the chunks coming from pinned host memory and, as a fast-link
+    case, from another device buffer.  Each schedule's merged result must equal, bit for bit, the
+    one computed with every chunk resident first."""
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
-    w = wl.WORKLOADS[2]
-    qr = w.query_rank
-    qmap = cpa.shard_layout(w.seq_len, w.cp, qr, w.layout)
-    q = wl.shard_tensor(w, "q", qr, device=dev)
-    host_k = [wl.shard_tensor(w, "k", r).pin_memory() for r in range(w.cp)]
-    host_v = [wl.shard_tensor(w, "v", r).pin_memory() for r in range(w.cp)]
-    compute, copy = torch.cuda.current_stream(), torch.cuda.Stream()
+    compute = torch.cuda.current_stream()
     results = []
-    sources = {"pinned_host": (host_k, host_v),
-               "device": ([t.to(dev) for t in host_k], [t.to(dev) for t in host_v])}
-    for source, (src_k, src_v) in sources.items():
-        for chunk_tokens in (512, 1024, 2048, 4096):
-            per_shard = w.local_len // chunk_tokens
-            n = w.cp * per_shard
-            order = wl.arrival_order(n, w.order_seed + 17 * qr)
-            chunks = []
-            for ci in order:
-                src, sub = divmod(int(ci), per_shard)
-                lo, hi = sub * chunk_tokens, (sub + 1) * chunk_tokens
-                kmap = cpa.sub_chunk_map(cpa.shard_layout(w.seq_len, w.cp, src, w.layout), sub, chunk_tokens)
-                chunks.append(dict(hk=src_k[src][lo:hi], hv=src_v[src][lo:hi], kmap=kmap,
-                                   dk=torch.empty((chunk_tokens, w.hkv, w.d), dtype=torch.bfloat16, device=dev),
-                                   dv=torch.empty((chunk_tokens, w.hkv, w.d), dtype=torch.bfloat16, device=dev),
-                                   o=torch.empty((w.local_len, w.hq, w.d), device=dev),
-                                   l=torch.empty((w.local_len, w.hq), device=dev)))
-            out = torch.empty((w.local_len, w.hq, w.d), dtype=torch.bfloat16, device=dev)
-            lse = torch.empty((w.local_len, w.hq), device=dev)
-            flops = sum(4 * w.d * w.hq * cpa.visible_pairs(qmap, w.local_len, c["kmap"], chunk_tokens) for c in chunks)
+    cases = [(2, (512, 1024, 2048, 4096)), (3, (2048, 4096, 8192))]
+    if args.config is not None:
+        cases = [c for c in cases if c[0] == args.config] or cases
 
-            # two receive buffers for the double-buffered schedule
-            ring = [(torch.empty_like(chunks[0]["dk"]), torch.empty_like(chunks[0]["dv"])) for _ in range(2)]
+    def timed(fn, reps):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(compute)
+        for _ in range(reps):
+            fn()
+        b.record(compute)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
 
-            def once(overlap):
-                evs = []
-                copy.wait_stream(compute)  # the receive buffers are free once the last step is done
-                with torch.cuda.stream(copy):
-                    for c in chunks:
-                        c["dk"].copy_(c["hk"], non_blocking=True)
-                        c["dv"].copy_(c["hv"], non_blocking=True)
-                        e = torch.cuda.Event()
-                        e.record(copy)
-                        evs.append(e)
-                if not overlap:
-                    compute.wait_event(evs[-1])
-                for c, e in zip(chunks, evs):
-                    compute.wait_event(e)
-                    cpa.partial_attn(q, c["dk"], c["dv"], qmap, c["kmap"], causal=True, o=c["o"], lse=c["l"])
-                cpa.merge_partials([c["o"] for c in chunks], [c["l"] for c in chunks], o=out, lse=lse)
-
-            def double_buffered():
-                # chunk i lands in ring[i % 2]; its copy waits until the partial of chunk i - 2 has
-                # consumed that buffer (an event on the compute stream)
-                copy.wait_stream(compute)
-                freed = [None, None]
-                for i, c in enumerate(chunks):
-                    dk, dv = ring[i % 2]
-                    with torch.cuda.stream(copy):
-                        if freed[i % 2] is not None:
-                            copy.wait_event(freed[i % 2])
-                        dk.copy_(c["hk"], non_blocking=True)
-                        dv.copy_(c["hv"], non_blocking=True)
-                        arrived = torch.cuda.Event()
-                        arrived.record(copy)
-                    compute.wait_event(arrived)
-                    cpa.partial_attn(q, dk, dv, qmap, c["kmap"], causal=True, o=c["o"], lse=c["l"])
-                    done = torch.cuda.Event()
-                    done.record(compute)
-                    freed[i % 2] = done
-                cpa.merge_partials([c["o"] for c in chunks], [c["l"] for c in chunks], o=out, lse=lse)
-
-            def timed(fn, reps):
-                for _ in range(args.warmup):
-                    fn()
-                torch.cuda.synchronize()
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(compute)
-                for _ in range(reps):
-                    fn()
-                b.record(compute)
-                torch.cuda.synchronize()
-                return a.elapsed_time(b) / reps
-
-            def copies_only():
-                copy.wait_stream(compute)
-                with torch.cuda.stream(copy):
-                    for c in chunks:
-                        c["dk"].copy_(c["hk"], non_blocking=True)
-                        c["dv"].copy_(c["hv"], non_blocking=True)
-                compute.wait_stream(copy)
-
-            def compute_only():
-                for c in chunks:
-                    cpa.partial_attn(q, c["dk"], c["dv"], qmap, c["kmap"], causal=True, o=c["o"], lse=c["l"])
-                cpa.merge_partials([c["o"] for c in chunks], [c["l"] for c in chunks], o=out, lse=lse)
-
-            t_copy = timed(copies_only, args.steps)
-            t_comp = timed(compute_only, args.steps)
-            t_serial = timed(lambda: once(False), args.steps)
-            t_pipe = timed(lambda: once(True), args.steps)
-            t_db = timed(double_buffered, args.steps)
-            # the schedules change only when each chunk's data lands: the merged result must be the
-            # same bits as with every chunk resident before the first partial
-            compute_only()
-            ref_out, ref_lse = out.clone(), lse.clone()
-            out.zero_(); lse.zero_()
-            double_buffered()
-            torch.cuda.synchronize()
-            same = bool(torch.equal(out, ref_out) and torch.equal(lse, ref_lse))
-            results.append({"source": source, "chunk_tokens": chunk_tokens, "chunks": n, "copy_ms": t_copy, "compute_ms": t_comp,
-                            "serial_ms": t_serial, "pipelined_ms": t_pipe,
-                            "overlap_gain": 1.0 - t_pipe / t_serial,
-                            "double_buffered_ms": t_db, "double_buffered_bit_identical": same,
-                            "ideal_ms": max(t_copy, t_comp),
-                            "TFLOP/s_pipelined": flops / (t_pipe * 1e-3) / 1e12})
-    best = min((r for r in results if r["source"] == "pinned_host"), key=lambda r: r["pipelined_ms"])
+    for cfg, sizes in cases:
+        for source in ("pinned_host", "device"):
+            for chunk_tokens in sizes:
+                ps = PipelinedStep(cfg, dev, chunk_tokens, source)
+                t_copy = timed(ps.copies_only, args.steps)
+                t_comp = timed(ps.compute_only, args.steps)
+                t_serial = timed(ps.serial, args.steps)
+                t_pipe = timed(ps.overlapped, args.steps)
+                t_db = timed(ps.double_buffered, args.steps)
+                # the schedules change only when each chunk's data lands
+                ps.compute_only()
+                ref_out, ref_lse = ps.out.clone(), ps.lse.clone()
+                same = True
+                for sched in (ps.overlapped, ps.double_buffered):
+                    ps.out.zero_()
+                    ps.lse.zero_()
+                    sched()
+                    torch.cuda.synchronize()
+                    same = same and bool(torch.equal(ps.out, ref_out) and torch.equal(ps.lse, ref_lse))
+                results.append({"workload": f"cfg{cfg}", "query_rank": ps.qr, "source": source,
+                                "chunk_tokens": chunk_tokens, "chunks": ps.n, "copy_ms": t_copy,
+                                "compute_ms": t_comp, "serial_ms": t_serial, "pipelined_ms": t_pipe,
+                                "overlap_gain": 1.0 - t_pipe / t_serial, "double_buffered_ms": t_db,
+                                "schedules_bit_identical": same, "ideal_ms": max(t_copy, t_comp),
+                                "TFLOP/s_pipelined": ps.flops / (t_pipe * 1e-3) / 1e12})
+                del ps, ref_out, ref_lse
+                torch.cuda.empty_cache()
+    head = [r for r in results if r["source"] == "pinned_host" and r["workload"] == f"cfg{cases[0][0]}"]
+    best = min(head, key=lambda r: r["pipelined_ms"])
+    from context_blockwise_attention_gb300 import workloads as wl
+    w = wl.WORKLOADS[cases[0][0]]
     line = {"metric": METRIC + " (chunk arrival overlapped with compute)",
             "value": best["TFLOP/s_pipelined"], "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": best["pipelined_ms"], "higher_is_better": True,
@@ -1036,7 +1173,7 @@ def run_pipelined(args):
             "data": "synthetic (seeded); chunks arrive by pinned host -> device copies on a second stream",
             "config": _config_dict(w, w.layout, {
                 "path": "partial per chunk as it arrives + merge", "chunks": best["chunks"],
-                "chunk_tokens": best["chunk_tokens"],
+                "chunk_tokens": best["chunk_tokens"], "query_rank": best["query_rank"],
                 "l2": "not flushed; each step copies all K/V chunks in and writes fp32 partials larger than L2"}),
             "pipeline": results}
     print(json.dumps(line), flush=True)
@@ -1045,9 +1182,15 @@ def run_pipelined(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--config", type=int, default=None, choices=[1, 2, 3, 4, 5],
+                    help="time one workload alone (default: workload 5 as the headline plus every "
+                         "workload in the line's configs object)")
+    ap.add_argument("--config-steps", type=int, default=20,
+                    help="timed steps per entry of the configs object (at most --steps)")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="default run without the configs object")
     ap.add_argument("--layout", default=None, choices=[None, "contiguous", "strided", "two_block", "balanced"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--ref-rows", type=int, default=0,
@@ -1070,6 +1213,8 @@ def main():
     if args.seq_len is not None:
         import dataclasses
         from context_blockwise_attention_gb300 import workloads as wl
+        if args.config is None:
+            ap.error("--seq-len needs --config")
         w = wl.WORKLOADS[args.config]
         wl.WORKLOADS[args.config] = dataclasses.replace(w, seq_len=args.seq_len)
     if args.impl == "reference":

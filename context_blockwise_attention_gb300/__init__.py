@@ -25,8 +25,6 @@ from .api import (  # noqa: F401
     library_path,
     load_library,
     version,
-    visible_pairs,
-    finite_rows,
 )
 
 __all__ = [
@@ -48,6 +46,4 @@ __all__ = [
     "library_path",
     "load_library",
     "version",
-    "visible_pairs",
-    "finite_rows",
 ]

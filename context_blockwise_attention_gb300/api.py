@@ -546,25 +546,3 @@ def ulysses_reshard(direction, tensors, cp, seq_len, layout="contiguous", out=No
     _check(lib.cp_ulysses_reshard(dirc, cp, seq_len, nt, arr_h, d, _dtype_code(dtype),
                                   _LAYOUTS[layout], arr_in, arr_out, _stream(stream)))
     return outs
-
-
-def visible_pairs(q_map: PosMap, n_q: int, k_map: PosMap, n_k: int, causal=True) -> int:
-    """Exact count of (query, key) pairs with kv_pos <= q_pos (for FLOP accounting)."""
-    import numpy as np
-    if not causal:
-        return int(n_q) * int(n_k)
-    qp = q_map.base + q_map.stride * np.arange(n_q, dtype=np.int64)
-    cnt = np.where(qp < k_map.base, 0, (qp - k_map.base) // k_map.stride + 1)
-    return int(np.minimum(cnt, n_k).sum())
-
-
-def finite_rows(q_map: PosMap, n_q: int, k_map: PosMap, n_k: int, causal=True) -> int:
-    """Number of query rows that see at least one key of the chunk (rows whose partial LSE is
-    finite); used for the merge's algorithmic byte count."""
-    import numpy as np
-    if n_k == 0:
-        return 0
-    if not causal:
-        return int(n_q)
-    qp = q_map.base + q_map.stride * np.arange(n_q, dtype=np.int64)
-    return int((qp >= k_map.base).sum())

@@ -10,8 +10,12 @@
 // The array is a module-scope __device__ variable: every device that loads the library holds
 // CP_NOALLOC_AUX_MAX_FLOATS floats (16 MiB) until the process exits.  Host code cannot use the
 // array's name as a device address (on the host it names a stand-in object), so the device
-// address is looked up with cudaGetSymbolAddress once per device, on the first call made with
-// that device current, and cached.
+// address is looked up with cudaGetSymbolAddress on the first call made with that device
+// current, and cached per device together with the identity of the CUDA context it belongs to.
+// With CUDA's lazy module loading that first lookup is also where the array is placed in device
+// memory, so the first call per device should be made at start-up.  If the context is destroyed
+// and recreated (cudaDeviceReset), the array moves: the next call sees a different context and
+// looks the address up again (placing the array again).
 
 #include <mutex>
 
@@ -25,8 +29,35 @@ namespace {
 
 constexpr int kMaxDev = 64;
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+template <typename Fn>
+Fn driver_fn(const char* name) {
+  void* ptr = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<Fn>(ptr);
+  return nullptr;
+}
+
+// Unique id of the calling thread's current context, or 0 if there is none (or it cannot be
+// read, in which case every call looks the address up again).
+unsigned long long current_ctx_id() {
+  static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
 std::mutex g_mu;
-float* g_aux_addr[kMaxDev];  // device address of g_noalloc_aux, per device, once looked up
+float* g_aux_addr[kMaxDev];              // device address of g_noalloc_aux, per device
+unsigned long long g_aux_ctx[kMaxDev];  // id of the context that address belongs to (0: none)
 
 }  // namespace
 
@@ -67,12 +98,15 @@ CP_API cp_status cp_partial_attn_bwd_noalloc(const cp_attn_bwd_desc* desc, const
   float* aux = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (g_aux_addr[dev] == nullptr) {
-      // first call on this device (which is current): the array's device address
+    const unsigned long long ctx = current_ctx_id();
+    if (g_aux_addr[dev] == nullptr || ctx == 0 || ctx != g_aux_ctx[dev]) {
+      // first call on this device (which is current), or its context changed since: the
+      // array's device address in the current context
       void* p = nullptr;
       const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_aux);
       if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(g_noalloc_aux)");
       g_aux_addr[dev] = static_cast<float*>(p);
+      g_aux_ctx[dev] = current_ctx_id();  // the lookup made the primary context current
     }
     aux = g_aux_addr[dev];
   }

@@ -372,8 +372,12 @@ cp_status cp_partial_attn_bwd_chunks(const cp_attn_bwd_desc* desc, int32_t n_chu
  * first call); nothing else needs to start at zero.
  * The workspace is one fixed array of CP_NOALLOC_AUX_MAX_FLOATS floats per device, held by every
  * device that loads the library until the process exits.  The first call on a device (with that
- * device current) looks up the array's device address; make that first call before any stream
- * capture.  Every call shares the array and leaves its contents behind: calls that may overlap on
+ * device current) looks up the array's device address; under CUDA's lazy module loading that
+ * lookup is also where the 16 MiB are placed in device memory, so it can fail with
+ * CP_ERR_CUDA (out of memory) inside a pool that owns all device memory: make that first call at
+ * start-up, before such a pool takes the memory and before any stream capture.  The address is
+ * cached per device with the identity of its CUDA context; after a cudaDeviceReset the next call
+ * looks it up again (and the array is placed again).  Every call shares the array and leaves its contents behind: calls that may overlap on
  * the GPU (different streams, or different host threads, without ordering between them) race on
  * it and give wrong gradients.  Calls on one stream are ordered and safe.
  * No cudaMalloc, cudaFree or other allocating call is made.

@@ -1,10 +1,11 @@
 """GPU parity at the benchmark workloads' full sizes, in the launch sequence bench.py times.
 
 Workloads 1 and 2: every row and head of every partial and of the merged output.
-Workloads 3-5: a seeded sample of query rows per rank (always including row 0, the last row,
-the rows on both sides of the first 128-row tile boundaries and, for workload 5, the first
+Workloads 3-5: a seeded sample of 256 query rows per rank (always including row 0, the last
+row, the rows on both sides of the first 128-row tile boundaries and, for workload 5, the first
 visible row of every chunk and the row just before it), all heads; every partial on the same
-rows.  The Ulysses reshards of workload 4 are compared bit for bit in full.
+rows.  Workload 4: 256 rows per head-rank.  The Ulysses reshards of workload 4 are compared bit
+for bit in full.
 """
 
 import numpy as np
@@ -107,11 +108,11 @@ def test_cfg2_rank0_sampled():
 
 @pytest.mark.parametrize("layout", ["strided", "contiguous", "two_block", "balanced"])
 def test_cfg3_all_ranks_sampled(layout):
-    _check_rank_workload(3, layout, 128)
+    _check_rank_workload(3, layout, 256)
 
 
 def test_cfg5_rank7_sampled_outliers():
-    _check_rank_workload(5, "strided", 128)
+    _check_rank_workload(5, "strided", 256)
 
 
 def _check_fused(cfg, layout, sample):
@@ -140,19 +141,26 @@ def test_cfg2_fused_full():
     _check_fused(2, "strided", None)
 
 
+@pytest.mark.parametrize("layout", ["strided", "contiguous"])
+def test_cfg3_fused_sampled(layout):
+    # every rank's query shard in one launch over its 8 chunks (contiguous: the chunks in the
+    # shard's future are not issued)
+    _check_fused(3, layout, 256)
+
+
 def test_cfg3_balanced_fused_sampled():
     # shards of equal causal work and unequal length, each query shard in one launch
-    _check_fused(3, "balanced", 128)
+    _check_fused(3, "balanced", 256)
 
 
 def test_cfg3_two_block_fused_sampled():
     # two query blocks per rank, each one launch over the 16 KV blocks visible to it
-    _check_fused(3, "two_block", 128)
+    _check_fused(3, "two_block", 256)
 
 
 def test_cfg5_fused_sampled():
     # 64 chunks with K outliers in one launch
-    _check_fused(5, "strided", 128)
+    _check_fused(5, "strided", 256)
 
 
 def test_cfg4_ulysses():
@@ -184,8 +192,9 @@ def test_cfg4_ulysses():
     back = oracle.head_to_seq(ints(gen), pos)
     for s in range(cp):
         assert np.array_equal(step.xo[s].cpu().view(i16).numpy(), back[s])
-    # the whole step again, then attention on sampled rows against the unsharded inputs:
-    # per head-rank output (head-sharded) and the final sequence-sharded output
+    # the whole step again, then attention on 256 sampled rows against the unsharded inputs:
+    # per head-rank O and LSE (head-sharded), and the final sequence-sharded O.  (The path's final
+    # product is O; LSE stays head-sharded, where the backward's three reversed exchanges use it.)
     for t in step.yo + step.ylse + step.xo:
         t.fill_(float("nan"))
     step.run()
@@ -194,7 +203,7 @@ def test_cfg4_ulysses():
     k_full = torch.cat([x.cpu() for x in step.ks])
     v_full = torch.cat([x.cpu() for x in step.vs])
     gpos = np.arange(S)
-    rows = wl.sample_rows(S, 96, seed=4, must=[0, 1, 127, 128, S - 1, S // 2])
+    rows = wl.sample_rows(S, 256, seed=4, must=[0, 1, 127, 128, S - 1, S // 2])
     idx = torch.from_numpy(rows).to(DEV)
     local = S // cp
     for r in range(cp):

@@ -1,10 +1,11 @@
-"""Seeded generators and the library-side FLOP accounting (CPU only)."""
+"""Seeded generators and the bench's FLOP accounting (CPU only)."""
 
 import numpy as np
 import torch
 
 import oracle
-from context_blockwise_attention_gb300 import PosMap, visible_pairs
+from bench import visible_pairs
+from context_blockwise_attention_gb300 import PosMap
 from context_blockwise_attention_gb300 import workloads as wl
 
 

@@ -6,18 +6,22 @@ inputs and outputs.  For them the library keeps the backward's per-row workspace
 array of its own.  These tests check, through the C ABI, that this entry point gives the same
 gradients as the ordinary two-call path (``cp_attn_bwd_prep`` into a caller-allocated workspace,
 then ``cp_partial_attn_bwd``), on several calls in a row with different shapes, so that what one
-call leaves in the shared array cannot leak into the next; and that sizes above the array's limit
-are refused with a clear message.
+call leaves in the shared array cannot leak into the next; that on one case its gradients match
+the CPU oracle's chain rule directly; that once the first call has placed the array, further calls
+leave the device's free memory unchanged; and that sizes above the array's limit are refused
+with a clear message.
 
 The file is named so that pytest collects it after every other test file.
 """
 
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
 import helpers
+import oracle
 from helpers import TOL_GRAD_BF16, TOL_GRAD_F32, compare_grad
 
 helpers.ensure_built()
@@ -90,6 +94,52 @@ def test_noalloc_matches_two_call_backward():
         tol = TOL_GRAD_BF16 if dtype == torch.bfloat16 else TOL_GRAD_F32
         for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
             compare_grad(g.cpu().numpy(), r.cpu().numpy(), tol, f"no-alloc {name} call {i} {case[:7]}")
+
+
+@pytest.mark.gpu
+def test_noalloc_matches_oracle():
+    # bf16 GQA 8/2, D=128, a causal chunk whose keys straddle the query shard's positions; the
+    # rows' final O and LSE come from the oracle (fp32) and feed both sides, so the comparison
+    # isolates the backward
+    dev = torch.device("cuda", 0)
+    sq, skv, hq, hkv, d = 200, 300, 8, 2, 128
+    qm, km = PosMap(150, 1), PosMap(0, 1)
+    q = wl.normal((sq, hq, d), torch.bfloat16, 501, device=dev)
+    k = wl.normal((skv, hkv, d), torch.bfloat16, 502, device=dev)
+    v = wl.normal((skv, hkv, d), torch.bfloat16, 503, device=dev)
+    d_o = wl.normal((sq, hq, d), torch.bfloat16, 504, device=dev)
+    qpos = qm.base + np.arange(sq)
+    kpos = km.base + np.arange(skv)
+    o_ref, l_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), qpos, kpos, causal=True)
+    o32 = torch.from_numpy(o_ref).float().to(dev)
+    l32 = torch.from_numpy(l_ref).float().to(dev)
+    got = [torch.zeros(t.shape, dtype=torch.float32, device=dev) for t in (q, k, v)]
+    cpa.partial_attn_bwd_noalloc(q, k, v, d_o, o32, l32, qm, km, *got, causal=True)
+    torch.cuda.synchronize()
+    ref = oracle.chunk_backward(q.cpu(), k.cpu(), v.cpu(), d_o.cpu(), o32.cpu(), l32.cpu(), qpos, kpos,
+                                causal=True)
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        compare_grad(g.cpu().numpy(), r, TOL_GRAD_BF16, f"no-alloc {name} vs oracle")
+
+
+@pytest.mark.gpu
+def test_noalloc_leaves_free_memory_unchanged():
+    # the first call on the device places the array (lazy module loading); after it, calls must
+    # not change the device's free memory (the library has its own CUDA runtime, so torch's
+    # allocator counters would not see an allocation: read the device's own figure)
+    dev = torch.device("cuda", 0)
+    case = _CASES[0]
+    q, k, v, d_o, o, lse = _inputs(case, 700, dev)
+    qm, km = case[7], case[8]
+    grads = [torch.zeros(t.shape, dtype=torch.float32, device=dev) for t in (q, k, v)]
+    cpa.partial_attn_bwd_noalloc(q, k, v, d_o, o, lse, qm, km, *grads, causal=True)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info(dev)
+    for _ in range(4):
+        cpa.partial_attn_bwd_noalloc(q, k, v, d_o, o, lse, qm, km, *grads, causal=True)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info(dev)
+    assert free1 == free0, f"free device memory changed by {free0 - free1} bytes"
 
 
 @pytest.mark.gpu
