@@ -1011,8 +1011,9 @@ class PipelinedStep:
         self.chunk_tokens = chunk_tokens
         self.qmap = cpa.shard_layout(w.seq_len, w.cp, qr, w.layout)
         self.q = wl.shard_tensor(w, "q", qr, device=device)
-        host_k = [wl.shard_tensor(w, "k", r) for r in range(w.cp)]
-        host_v = [wl.shard_tensor(w, "v", r) for r in range(w.cp)]
+        # K and V are drawn on the host (they arrive from there); Q on the device
+        host_k = self.host_k = [wl.shard_tensor(w, "k", r) for r in range(w.cp)]
+        host_v = self.host_v = [wl.shard_tensor(w, "v", r) for r in range(w.cp)]
         if source == "pinned_host":
             src_k, src_v = [t.pin_memory() for t in host_k], [t.pin_memory() for t in host_v]
         else:

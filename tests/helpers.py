@@ -60,6 +60,13 @@ def compare_partial(o_gpu, l_gpu, o_ref, l_ref, tol_o, tol_l, what=""):
 # 2^-9 each) before the dV, dK and dQ products.
 TOL_GRAD_F32 = 1e-5
 TOL_GRAD_BF16 = 1e-2
+# bf16 inputs, also per row: every gradient row (one token and head, all D columns) is checked
+# against its own scale, max|ref row|, so an error in a row far smaller than the tensor's peak
+# cannot hide under the tensor-wide bound; rows below 1e-3 of the tensor's scale are held to that
+# floor instead (their reference is dominated by cancellation).  Observed worst over the parity
+# cases: 4.3e-3.
+TOL_GRAD_BF16_ROW = 1e-2
+ROW_FLOOR = 1e-3
 
 
 def compare_grad(g_gpu, g_ref, tol, what=""):
@@ -70,5 +77,12 @@ def compare_grad(g_gpu, g_ref, tol, what=""):
     scale = max(1.0, float(np.abs(g_ref).max()) if g_ref.size else 1.0)
     err = float(np.abs(g_gpu - g_ref).max()) / scale if g_ref.size else 0.0
     assert err <= tol, f"{what}: max|err|/scale = {err:.3e} > {tol} (scale {scale:.3g})"
+    if tol == TOL_GRAD_BF16 and g_ref.size:
+        rows_err = np.abs(g_gpu - g_ref).max(axis=-1)
+        rows_scale = np.maximum(np.abs(g_ref).max(axis=-1), ROW_FLOOR * float(np.abs(g_ref).max()))
+        live = rows_scale > 0
+        rel = float((rows_err[live] / rows_scale[live]).max()) if live.any() else 0.0
+        assert np.all(rows_err[~live] == 0.0), f"{what}: rows with a zero reference must be exactly zero"
+        assert rel <= TOL_GRAD_BF16_ROW, f"{what}: worst row max|err|/max|ref row| = {rel:.3e} > {TOL_GRAD_BF16_ROW}"
     return err
 

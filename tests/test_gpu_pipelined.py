@@ -26,20 +26,16 @@ from context_blockwise_attention_gb300 import workloads as wl  # noqa: E402
 
 DEV = torch.device("cuda", 0) if torch.cuda.is_available() else None
 
-_REF = {}
-
-
-def _reference(cfg, qr, rows):
-    """Oracle O and LSE of the sampled rows of query rank qr over every key of the workload."""
-    key = (cfg, qr)
-    if key not in _REF:
-        w = wl.WORKLOADS[cfg]
-        pos = [oracle.shard_positions(w.seq_len, w.cp, r, w.layout) for r in range(w.cp)]
-        k = torch.cat([wl.shard_tensor(w, "k", r) for r in range(w.cp)])
-        v = torch.cat([wl.shard_tensor(w, "v", r) for r in range(w.cp)])
-        q = wl.shard_tensor(w, "q", qr)[torch.from_numpy(rows)]
-        _REF[key] = oracle.attention(q, k, v, pos[qr][rows], np.concatenate(pos), causal=w.causal)
-    return _REF[key]
+def _reference(ps, rows):
+    """Oracle O and LSE of the sampled rows of the step's query shard over every key of the
+    workload, from the very tensors the step holds (its Q from the device, K and V from the host
+    copies the chunks arrive from)."""
+    w = ps.w
+    pos = [oracle.shard_positions(w.seq_len, w.cp, r, w.layout) for r in range(w.cp)]
+    k = torch.cat(ps.host_k)
+    v = torch.cat(ps.host_v)
+    q = ps.q.cpu()[torch.from_numpy(rows)]
+    return oracle.attention(q, k, v, pos[ps.qr][rows], np.concatenate(pos), causal=w.causal)
 
 
 @pytest.mark.parametrize("cfg,chunk_tokens,source", [
@@ -50,7 +46,7 @@ def test_pipelined_schedules_match_oracle(cfg, chunk_tokens, source):
     assert ps.n == w.cp * (w.local_len // chunk_tokens)
     rows = wl.sample_rows(w.local_len, 256, seed=chunk_tokens + cfg,
                           must=[0, 127, 128, w.local_len - 1])
-    o_ref, l_ref = _reference(cfg, ps.qr, rows)
+    o_ref, l_ref = _reference(ps, rows)
     idx = torch.from_numpy(rows).to(DEV)
     for name in ("serial", "overlapped", "double_buffered"):
         # poison every partial and the merged output so rows a schedule skipped cannot pass
