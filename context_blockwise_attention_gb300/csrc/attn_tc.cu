@@ -280,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
       // ============================================================== TMA producer
       const bool leader = ptx::elect_one();
+      const uint32_t lead = leader ? 1u : 0u;
       if (leader) {
         ptx::tma_prefetch_desc(&tm_q);
         for (int c = 0; c < ch.n; ++c) {
@@ -305,35 +306,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int st = static_cast<int>(gj % L::kStages);
             const uint32_t ph = static_cast<uint32_t>((gj / L::kStages) & 1);
             if (!(ok = wait_warp(b.k_empty + 8 * st, ph ^ 1, ctl, kSiteKEmpty))) break;
-            if (leader) {
-              ptx::mbar_arrive_expect_tx(b.k_full + 8 * st, L::kTileBytes);
-              for (int cc = 0; cc < L::kChunks; ++cc)
-                ptx::tma_load_2d(sK + st * L::kTileBytes + cc * L::kChunkBytes, &ch.k[c], w.kvh * D + cc * 64,
-                                 t * kKeys, b.k_full + 8 * st);
-          }
+            ptx::mbar_arrive_expect_tx_p(b.k_full + 8 * st, L::kTileBytes, lead);
+#pragma unroll
+            for (int cc = 0; cc < L::kChunks; ++cc)
+              ptx::tma_load_2d_p(sK + st * L::kTileBytes + cc * L::kChunkBytes, &ch.k[c], w.kvh * D + cc * 64,
+                                 t * kKeys, b.k_full + 8 * st, lead);
           __syncwarp();
           kl = gj + 1;
           if (j == 0) {
             // the Q buffer is free once every QK of the previous unit has completed
             if (kq > 0 && !(ok = wait_warp(b.q_empty, static_cast<uint32_t>((kq - 1) & 1), ctl, kSiteQEmpty)))
               break;
-            if (leader) {
-              ptx::mbar_arrive_expect_tx(b.q_full, 2 * L::kTileBytes);
-              for (int x = 0; x < 2; ++x)
-                for (int cc = 0; cc < L::kChunks; ++cc)
-                  ptx::tma_load_2d(sQ + x * L::kTileBytes + cc * L::kChunkBytes, &tm_q, w.h * D + cc * 64,
-                                   static_cast<int32_t>(w.row0 + x * kRows), b.q_full);
-            }
+            ptx::mbar_arrive_expect_tx_p(b.q_full, 2 * L::kTileBytes, lead);
+#pragma unroll
+            for (int x = 0; x < 2; ++x)
+#pragma unroll
+              for (int cc = 0; cc < L::kChunks; ++cc)
+                ptx::tma_load_2d_p(sQ + x * L::kTileBytes + cc * L::kChunkBytes, &tm_q, w.h * D + cc * 64,
+                                   static_cast<int32_t>(w.row0 + x * kRows), b.q_full, lead);
             __syncwarp();
             ql = kq + 1;
           }
           if (!(ok = wait_warp(b.v_empty + 8 * st, ph ^ 1, ctl, kSiteVEmpty))) break;
-          if (leader) {
-            ptx::mbar_arrive_expect_tx(b.v_full + 8 * st, L::kTileBytes);
-            for (int cc = 0; cc < L::kChunks; ++cc)
-              ptx::tma_load_2d(sV + st * L::kTileBytes + cc * L::kChunkBytes, &ch.v[c], w.kvh * D + cc * 64,
-                               t * kKeys, b.v_full + 8 * st);
-          }
+          ptx::mbar_arrive_expect_tx_p(b.v_full + 8 * st, L::kTileBytes, lead);
+#pragma unroll
+          for (int cc = 0; cc < L::kChunks; ++cc)
+            ptx::tma_load_2d_p(sV + st * L::kTileBytes + cc * L::kChunkBytes, &ch.v[c], w.kvh * D + cc * 64,
+                               t * kKeys, b.v_full + 8 * st, lead);
           __syncwarp();
           vl = gj + 1;
           }
@@ -357,6 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ============================================================== MMA issuer
       // The whole warp runs the loop and waits; one elected lane issues each tcgen05 instruction.
       const bool leader = ptx::elect_one();
+      const uint32_t lead = leader ? 1u : 0u;
       constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(kRows, kKeys, 0, 0);
       constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kRows, D, 0, 1);
       // descriptor bases (start address field counts 16-byte units)
@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = static_cast<uint64_t>(((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4);
-          ptx::mma_ss(tmem + x * 128u, qd + off, kd + off, kIdescQK, kk > 0 ? 1u : 0u);
+          ptx::mma_ss_p(tmem + x * 128u, qd + off, kd + off, kIdescQK, kk > 0 ? 1u : 0u, lead);
         }
       };
       auto issue_pv = [&](int x, int st, int half, bool acc) {
@@ -381,8 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int kk = half * 4 + q;
-          ptx::mma_ts(tmem + 256u + x * 128u, tmem + x * 128u + kk * 8, vd + static_cast<uint64_t>(kk * 128),
-                      kIdescPV, (acc || kk > 0) ? 1u : 0u);
+          ptx::mma_ts_p(tmem + 256u + x * 128u, tmem + x * 128u + kk * 8, vd + static_cast<uint64_t>(kk * 128),
+                        kIdescPV, (acc || kk > 0) ? 1u : 0u, lead);
         }
       };
       // PV for Q tile x with the V tile of global step gg (stage st): first half as soon as P's
@@ -394,11 +394,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           return false;
         if (!wait_warp(b.p_half + 8 * x, static_cast<uint32_t>(gg & 1), ctl, kSitePFull)) return false;
         ptx::tc_fence_after();
-        if (leader) issue_pv(x, st, 0, !first);
+        issue_pv(x, st, 0, !first);
         __syncwarp();
         if (!wait_warp(b.p_full + 8 * x, static_cast<uint32_t>(gg & 1), ctl, kSitePFull)) return false;
         ptx::tc_fence_after();
-        if (leader) issue_pv(x, st, 1, true);
+        issue_pv(x, st, 1, true);
         __syncwarp();
         return true;
       };
@@ -417,28 +417,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t ph = static_cast<uint32_t>((gj / L::kStages) & 1);
           if (!(ok = wait_warp(b.k_full + 8 * st, ph, ctl, kSiteKFull))) break;
           ptx::tc_fence_after();
-          if (leader) {
-            issue_qk(0, st);
-            ptx::mma_commit(b.s_full);
-          }
+          issue_qk(0, st);
+          ptx::mma_commit_p(b.s_full, lead);
           __syncwarp();
           if (j > 0) {
             const int pst = static_cast<int>((gj - 1) % L::kStages);
             if (!(ok = pv_tile(1, pst, gj - 1, j - 1 == 0, kq))) break;
-            if (leader) ptx::mma_commit(b.v_empty + 8 * pst);
+            ptx::mma_commit_p(b.v_empty + 8 * pst, lead);
             __syncwarp();
           }
-          if (leader) {
-            issue_qk(1, st);
-            ptx::mma_commit(b.s_full + 8);
-            ptx::mma_commit(b.k_empty + 8 * st);
-            if (j == n - 1) ptx::mma_commit(b.q_empty);  // every QK of this unit issued
-          }
+          issue_qk(1, st);
+          ptx::mma_commit_p(b.s_full + 8, lead);
+          ptx::mma_commit_p(b.k_empty + 8 * st, lead);
+          if (j == n - 1) ptx::mma_commit_p(b.q_empty, lead);  // every QK of this unit issued
           __syncwarp();
           if (!(ok = wait_warp(b.v_full + 8 * st, ph, ctl, kSiteVFull))) break;
           if (!(ok = pv_tile(0, st, gj, j == 0, kq))) break;
           if (j == n - 1) {
-            if (leader) ptx::mma_commit(b.o_final);
+            ptx::mma_commit_p(b.o_final, lead);
             __syncwarp();
           }
         }
@@ -447,10 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int64_t gl = g + n - 1;
           const int st = static_cast<int>(gl % L::kStages);
           if (!(ok = pv_tile(1, st, gl, n == 1, kq))) break;
-          if (leader) {
-            ptx::mma_commit(b.v_empty + 8 * st);
-            ptx::mma_commit(b.o_final + 8);
-          }
+          ptx::mma_commit_p(b.v_empty + 8 * st, lead);
+          ptx::mma_commit_p(b.o_final + 8, lead);
           __syncwarp();
         }
         g += n;
