@@ -187,6 +187,34 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, const ChunkTable<
   return w;
 }
 
+// Issue of MMAs, commits and TMA copies by the control warps: at D = 128 the converged warp issues
+// under a lane predicate (the MMA issue rate bounds that head dim; measured +10 %), at D = 64 the
+// elected lane alone (measured 2-4 % faster there).
+template <bool kPred>
+struct Issue {
+  uint32_t lead;
+  __device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) const {
+    if (kPred) ptx::mma_ss_p(d, a, b, idesc, acc, lead);
+    else if (lead) ptx::mma_ss(d, a, b, idesc, acc);
+  }
+  __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) const {
+    if (kPred) ptx::mma_ts_p(d, a, b, idesc, acc, lead);
+    else if (lead) ptx::mma_ts(d, a, b, idesc, acc);
+  }
+  __device__ __forceinline__ void commit(uint32_t bar) const {
+    if (kPred) ptx::mma_commit_p(bar, lead);
+    else if (lead) ptx::mma_commit(bar);
+  }
+  __device__ __forceinline__ void expect_tx(uint32_t bar, uint32_t bytes) const {
+    if (kPred) ptx::mbar_arrive_expect_tx_p(bar, bytes, lead);
+    else if (lead) ptx::mbar_arrive_expect_tx(bar, bytes);
+  }
+  __device__ __forceinline__ void load(uint32_t dst, const void* tmap, int32_t x, int32_t y, uint32_t bar) const {
+    if (kPred) ptx::tma_load_2d_p(dst, tmap, x, y, bar, lead);
+    else if (lead) ptx::tma_load_2d(dst, tmap, x, y, bar);
+  }
+};
+
 // exp2 of 32 scaled scores (x = s * sl2 - m) packed to 16 bf16 pairs; adds the fp32 values to
 // the two packed partial sums.  (Evaluating part of the exponentials with a polynomial on the FMA
 // pipe was measured slower on GB300 for both head dims: the softmax is bound by instruction issue
@@ -280,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
       // ============================================================== TMA producer
       const bool leader = ptx::elect_one();
-      const uint32_t lead = leader ? 1u : 0u;
+      const Issue<D == 128> is{leader ? 1u : 0u};
       if (leader) {
         ptx::tma_prefetch_desc(&tm_q);
         for (int c = 0; c < ch.n; ++c) {
@@ -306,33 +334,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int st = static_cast<int>(gj % L::kStages);
             const uint32_t ph = static_cast<uint32_t>((gj / L::kStages) & 1);
             if (!(ok = wait_warp(b.k_empty + 8 * st, ph ^ 1, ctl, kSiteKEmpty))) break;
-            ptx::mbar_arrive_expect_tx_p(b.k_full + 8 * st, L::kTileBytes, lead);
+            is.expect_tx(b.k_full + 8 * st, L::kTileBytes);
 #pragma unroll
             for (int cc = 0; cc < L::kChunks; ++cc)
-              ptx::tma_load_2d_p(sK + st * L::kTileBytes + cc * L::kChunkBytes, &ch.k[c], w.kvh * D + cc * 64,
-                                 t * kKeys, b.k_full + 8 * st, lead);
+              is.load(sK + st * L::kTileBytes + cc * L::kChunkBytes, &ch.k[c], w.kvh * D + cc * 64, t * kKeys,
+                      b.k_full + 8 * st);
           __syncwarp();
           kl = gj + 1;
           if (j == 0) {
             // the Q buffer is free once every QK of the previous unit has completed
             if (kq > 0 && !(ok = wait_warp(b.q_empty, static_cast<uint32_t>((kq - 1) & 1), ctl, kSiteQEmpty)))
               break;
-            ptx::mbar_arrive_expect_tx_p(b.q_full, 2 * L::kTileBytes, lead);
+            is.expect_tx(b.q_full, 2 * L::kTileBytes);
 #pragma unroll
             for (int x = 0; x < 2; ++x)
 #pragma unroll
               for (int cc = 0; cc < L::kChunks; ++cc)
-                ptx::tma_load_2d_p(sQ + x * L::kTileBytes + cc * L::kChunkBytes, &tm_q, w.h * D + cc * 64,
-                                   static_cast<int32_t>(w.row0 + x * kRows), b.q_full, lead);
+                is.load(sQ + x * L::kTileBytes + cc * L::kChunkBytes, &tm_q, w.h * D + cc * 64,
+                        static_cast<int32_t>(w.row0 + x * kRows), b.q_full);
             __syncwarp();
             ql = kq + 1;
           }
           if (!(ok = wait_warp(b.v_empty + 8 * st, ph ^ 1, ctl, kSiteVEmpty))) break;
-          ptx::mbar_arrive_expect_tx_p(b.v_full + 8 * st, L::kTileBytes, lead);
+          is.expect_tx(b.v_full + 8 * st, L::kTileBytes);
 #pragma unroll
           for (int cc = 0; cc < L::kChunks; ++cc)
-            ptx::tma_load_2d_p(sV + st * L::kTileBytes + cc * L::kChunkBytes, &ch.v[c], w.kvh * D + cc * 64,
-                               t * kKeys, b.v_full + 8 * st, lead);
+            is.load(sV + st * L::kTileBytes + cc * L::kChunkBytes, &ch.v[c], w.kvh * D + cc * 64, t * kKeys,
+                    b.v_full + 8 * st);
           __syncwarp();
           vl = gj + 1;
           }
@@ -356,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ============================================================== MMA issuer
       // The whole warp runs the loop and waits; one elected lane issues each tcgen05 instruction.
       const bool leader = ptx::elect_one();
-      const uint32_t lead = leader ? 1u : 0u;
+      const Issue<D == 128> is{leader ? 1u : 0u};
       constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(kRows, kKeys, 0, 0);
       constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kRows, D, 0, 1);
       // descriptor bases (start address field counts 16-byte units)
@@ -373,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = static_cast<uint64_t>(((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4);
-          ptx::mma_ss_p(tmem + x * 128u, qd + off, kd + off, kIdescQK, kk > 0 ? 1u : 0u, lead);
+          is.mma_ss(tmem + x * 128u, qd + off, kd + off, kIdescQK, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int x, int st, int half, bool acc) {
@@ -381,8 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int kk = half * 4 + q;
-          ptx::mma_ts_p(tmem + 256u + x * 128u, tmem + x * 128u + kk * 8, vd + static_cast<uint64_t>(kk * 128),
-                        kIdescPV, (acc || kk > 0) ? 1u : 0u, lead);
+          is.mma_ts(tmem + 256u + x * 128u, tmem + x * 128u + kk * 8, vd + static_cast<uint64_t>(kk * 128),
+                    kIdescPV, (acc || kk > 0) ? 1u : 0u);
         }
       };
       // PV for Q tile x with the V tile of global step gg (stage st): first half as soon as P's
@@ -418,23 +446,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = wait_warp(b.k_full + 8 * st, ph, ctl, kSiteKFull))) break;
           ptx::tc_fence_after();
           issue_qk(0, st);
-          ptx::mma_commit_p(b.s_full, lead);
+          is.commit(b.s_full);
           __syncwarp();
           if (j > 0) {
             const int pst = static_cast<int>((gj - 1) % L::kStages);
             if (!(ok = pv_tile(1, pst, gj - 1, j - 1 == 0, kq))) break;
-            ptx::mma_commit_p(b.v_empty + 8 * pst, lead);
+            is.commit(b.v_empty + 8 * pst);
             __syncwarp();
           }
           issue_qk(1, st);
-          ptx::mma_commit_p(b.s_full + 8, lead);
-          ptx::mma_commit_p(b.k_empty + 8 * st, lead);
-          if (j == n - 1) ptx::mma_commit_p(b.q_empty, lead);  // every QK of this unit issued
+          is.commit(b.s_full + 8);
+          is.commit(b.k_empty + 8 * st);
+          if (j == n - 1) is.commit(b.q_empty);  // every QK of this unit issued
           __syncwarp();
           if (!(ok = wait_warp(b.v_full + 8 * st, ph, ctl, kSiteVFull))) break;
           if (!(ok = pv_tile(0, st, gj, j == 0, kq))) break;
           if (j == n - 1) {
-            ptx::mma_commit_p(b.o_final, lead);
+            is.commit(b.o_final);
             __syncwarp();
           }
         }
@@ -443,8 +471,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int64_t gl = g + n - 1;
           const int st = static_cast<int>(gl % L::kStages);
           if (!(ok = pv_tile(1, st, gl, n == 1, kq))) break;
-          ptx::mma_commit_p(b.v_empty + 8 * st, lead);
-          ptx::mma_commit_p(b.o_final + 8, lead);
+          is.commit(b.v_empty + 8 * st);
+          is.commit(b.o_final + 8);
           __syncwarp();
         }
         g += n;

@@ -225,8 +225,9 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 
 // ------------------------------------------------------------------ predicated issue
 // Executed by every lane of a converged warp; only the lane with lead != 0 issues.  On sm_103a a
-// warp issues tcgen05.mma, tcgen05.commit and TMA copies much faster this way than from a branch
-// only one lane enters (measured: 8 MMAs in ~156 cycles against ~400).
+// warp issues tcgen05.mma back to back much faster this way than from a branch only one lane
+// enters (measured: 8 MMAs in ~156 cycles against ~400); whether that helps depends on the
+// kernel's schedule, so the kernels choose.
 __device__ __forceinline__ void mma_ss_p(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate, uint32_t lead) {
   asm volatile(
@@ -273,17 +274,6 @@ __device__ __forceinline__ void tma_load_2d_p(uint32_t dst, const void* tmap, in
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "r"(lead)
       : "memory");
 }
-__device__ __forceinline__ void tma_reduce_add_2d_p(const void* tmap, uint32_t src, int32_t x, int32_t y,
-                                                    uint32_t lead) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t"
-      "setp.ne.b32 e, %4, 0;\n\t"
-      "@e cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];\n\t}" ::"l"(
-          reinterpret_cast<uint64_t>(tmap)),
-      "r"(src), "r"(x), "r"(y), "r"(lead)
-      : "memory");
-}
-
 // ------------------------------------------------------------------ descriptors
 // Shared-memory matrix descriptor for tcgen05.mma, 128-byte swizzle.
 //   bits  0-13  start address >> 4

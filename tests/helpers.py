@@ -62,14 +62,16 @@ TOL_GRAD_F32 = 1e-5
 TOL_GRAD_BF16 = 1e-2
 # bf16 inputs, also per row: every gradient row (one token and head, all D columns) is checked
 # against its own scale, max|ref row|, so an error in a row far smaller than the tensor's peak
-# cannot hide under the tensor-wide bound; rows below 1e-3 of the tensor's scale are held to that
-# floor instead (their reference is dominated by cancellation).  Observed worst over the parity
-# cases: 4.3e-3.
+# cannot hide under the tensor-wide bound.  The rounding of P and dS bounds a row's error by 2^-9
+# of the magnitudes of the terms it sums, not of its value: a row whose terms cancel (a causal
+# query's first keys, where sum_j dS_ij = 0 holds with few terms) can be far below them, so rows
+# below 1e-2 of the tensor's scale are held to that floor (1e-4 of the tensor's scale).
+# Observed worst over the parity cases: 4.3e-3.
 TOL_GRAD_BF16_ROW = 1e-2
-ROW_FLOOR = 1e-3
+ROW_FLOOR = 1e-2
 
 
-def compare_grad(g_gpu, g_ref, tol, what=""):
+def compare_grad(g_gpu, g_ref, tol, what="", rows=True):
     g_gpu = np.asarray(g_gpu, dtype=np.float64)
     g_ref = np.asarray(g_ref, dtype=np.float64)
     assert g_gpu.shape == g_ref.shape, f"{what}: shape {g_gpu.shape} != {g_ref.shape}"
@@ -77,7 +79,7 @@ def compare_grad(g_gpu, g_ref, tol, what=""):
     scale = max(1.0, float(np.abs(g_ref).max()) if g_ref.size else 1.0)
     err = float(np.abs(g_gpu - g_ref).max()) / scale if g_ref.size else 0.0
     assert err <= tol, f"{what}: max|err|/scale = {err:.3e} > {tol} (scale {scale:.3g})"
-    if tol == TOL_GRAD_BF16 and g_ref.size:
+    if rows and tol == TOL_GRAD_BF16 and g_ref.size:
         rows_err = np.abs(g_gpu - g_ref).max(axis=-1)
         rows_scale = np.maximum(np.abs(g_ref).max(axis=-1), ROW_FLOOR * float(np.abs(g_ref).max()))
         live = rows_scale > 0
