@@ -394,6 +394,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
       // ============================================================== MMA issuer
       const bool leader = ptx::elect_one();
+      // How the MMAs are issued (measured per head dim, same-box A/B): at D = 128 a group of MMAs
+      // is issued inside one branch the elected lane takes; at D = 64 the converged warp runs the
+      // issue code and each MMA is guarded by its own elected-lane test (2.5 % faster there, 6 %
+      // slower at D = 128).
+      constexpr bool kGroupIssue = (D == 128);
+      const bool issuer = kGroupIssue ? leader : true;
       constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kKeys, kRows, 0, 0);  // S^T, dP^T
       constexpr uint32_t kIdescG = ptx::idesc_bf16_f32(kKeys, D, 0, 1);      // dV, dK (A in TMEM)
       constexpr uint32_t kIdescQ = ptx::idesc_bf16_f32(kRows, D, 1, 1);      // dQ (A = dS, MN-major)
@@ -412,22 +418,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = static_cast<uint64_t>(((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4);
-          ptx::mma_ss(d_tmem, a0 + off, b0 + off, kIdescS, kk > 0 ? 1u : 0u);
+          if (kGroupIssue || leader) ptx::mma_ss(d_tmem, a0 + off, b0 + off, kIdescS, kk > 0 ? 1u : 0u);
         }
       };
       // M=128 keys, N=D, K=128 queries: A (bf16 packed, 8 columns per 16 queries) in tensor memory
       auto issue_ts = [&](uint32_t d_tmem, uint32_t a_tmem, uint64_t b_mn, bool acc) {
 #pragma unroll
         for (int kk = 0; kk < kRows / 16; ++kk)
-          ptx::mma_ts(d_tmem, a_tmem + kk * 8, b_mn + static_cast<uint64_t>(kk * 128), kIdescG,
-                      (acc || kk > 0) ? 1u : 0u);
+          if (kGroupIssue || leader)
+            ptx::mma_ts(d_tmem, a_tmem + kk * 8, b_mn + static_cast<uint64_t>(kk * 128), kIdescG,
+                        (acc || kk > 0) ? 1u : 0u);
       };
       // M=128 queries, N=D, K=128 keys: dS (MN-major) x K (MN-major)
       auto issue_dq = [&](uint32_t d_tmem) {
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk)
-          ptx::mma_ss(d_tmem, dDS_mn + static_cast<uint64_t>(kk * 128), dK_mn + static_cast<uint64_t>(kk * 128),
-                      kIdescQ, kk > 0 ? 1u : 0u);
+          if (kGroupIssue || leader)
+            ptx::mma_ss(d_tmem, dDS_mn + static_cast<uint64_t>(kk * 128), dK_mn + static_cast<uint64_t>(kk * 128),
+                        kIdescQ, kk > 0 ? 1u : 0u);
       };
 
       // Per query tile gi of a unit: [S^T(gi) if first of the unit] dP^T(gi), dV(gi), S^T(gi+1) of
@@ -436,10 +444,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sq = static_cast<int>(g % L::kQStages);
         if (!wait_warp(b.q_full + 8 * sq, static_cast<uint32_t>((g / L::kQStages) & 1), ctl, kSQFull)) return false;
         ptx::tc_fence_after();
-        if (leader) {
-          issue_kk(tmem + L::kColS, dK_k, dQ_k + sq * kTileUnits);
-          ptx::mma_commit(b.s_full);
-        }
+        if (issuer) issue_kk(tmem + L::kColS, dK_k, dQ_k + sq * kTileUnits);
+        if (leader) ptx::mma_commit(b.s_full);
         __syncwarp();
         return true;
       };
@@ -464,31 +470,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           // D = 128: the previous dQ sits in the dP^T columns until the reduction warps read it
           if (D == 128 && gi > 0 && !(ok = wait_warp(b.dq_free, prev, ctl, kSDqFree))) break;
           ptx::tc_fence_after();
-          if (leader) {
-            issue_kk(tmem + L::kColDP, dV_k, dDO_k + sd * kTileUnits);
-            ptx::mma_commit(b.dp_full);
-          }
+          if (issuer) issue_kk(tmem + L::kColDP, dV_k, dDO_k + sd * kTileUnits);
+          if (leader) ptx::mma_commit(b.dp_full);
           __syncwarp();
           if (!(ok = wait_warp(b.p_ready, cur, ctl, kSPReady))) break;
           // the unit's first dV overwrites the accumulators: the previous unit's must be read out
           if (first && ku > 0 && !(ok = wait_warp(b.acc_empty, static_cast<uint32_t>((ku - 1) & 1), ctl, kSAccEmpty)))
             break;
           ptx::tc_fence_after();
-          if (leader) {
-            issue_ts(tmem + L::kColDV, tmem + L::kColS, dDO_mn + sd * kTileUnits, !first);
-            ptx::mma_commit(b.do_empty + 8 * sd);
-          }
+          if (issuer) issue_ts(tmem + L::kColDV, tmem + L::kColS, dDO_mn + sd * kTileUnits, !first);
+          if (leader) ptx::mma_commit(b.do_empty + 8 * sd);
           __syncwarp();
           // the next S^T may overwrite P^T: the dV product just issued reads it first (issue order)
           if (it + 1 < w.nit && !(ok = issue_s(gi + 1))) break;
           if (!(ok = wait_warp(b.ds_ready, cur, ctl, kSDsReady))) break;
           ptx::tc_fence_after();
-          if (leader) issue_ts(tmem + L::kColDK, tmem + L::kColDP, dQ_mn + st * kTileUnits, !first);
+          if (issuer) issue_ts(tmem + L::kColDK, tmem + L::kColDP, dQ_mn + st * kTileUnits, !first);
           __syncwarp();
           if (D == 64 && gi > 0 && !(ok = wait_warp(b.dq_free, prev, ctl, kSDqFree))) break;
           ptx::tc_fence_after();
+          if (issuer) issue_dq(tmem + L::kColDQ);
           if (leader) {
-            issue_dq(tmem + L::kColDQ);
             ptx::mma_commit(b.dq_full);
             ptx::mma_commit(b.q_empty + 8 * st);
             if (it == w.nit - 1) {
