@@ -240,6 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ BwdChunks<MAXC> ch) {
   using L = BLayout<D>;
   using namespace sync;
+  // bounded waits probe the phase with test_wait first at D = 64 (measured faster there)
+  constexpr bool kProbe = (D == 64);
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -333,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (u >= p.n_units) break;
         const BUnit w = decode_bunit(p, ch, u);
         if (w.nit <= 0) continue;
-        if (ku > 0 && !(ok = wait_warp(b.kv_empty, static_cast<uint32_t>((ku - 1) & 1), ctl, kSKvEmpty))) break;
+        if (ku > 0 && !(ok = wait_warp<kProbe>(b.kv_empty, static_cast<uint32_t>((ku - 1) & 1), ctl, kSKvEmpty))) break;
         if (leader) {
           ptx::mbar_arrive_expect_tx(b.kv_full, 2 * L::kTileBytes);
           for (int cc = 0; cc < L::kChunks; ++cc) {
@@ -346,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int t = w.t0 + it;
           const int st = static_cast<int>(gi % L::kQStages);
           const uint32_t ph = static_cast<uint32_t>((gi / L::kQStages) & 1);
-          if (!(ok = wait_warp(b.q_empty + 8 * st, ph ^ 1, ctl, kSQEmpty))) break;
+          if (!(ok = wait_warp<kProbe>(b.q_empty + 8 * st, ph ^ 1, ctl, kSQEmpty))) break;
           if (leader) {
             const uint32_t full = b.q_full + 8 * st;
             ptx::mbar_arrive_expect_tx(full, L::kTileBytes + 1024);
@@ -362,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ql = gi + 1;
           const int sd = static_cast<int>(gi % L::kDoStages);
           const uint32_t phd = static_cast<uint32_t>((gi / L::kDoStages) & 1);
-          if (!(ok = wait_warp(b.do_empty + 8 * sd, phd ^ 1, ctl, kSDoEmpty))) break;
+          if (!(ok = wait_warp<kProbe>(b.do_empty + 8 * sd, phd ^ 1, ctl, kSDoEmpty))) break;
           if (leader) {
             const uint32_t full = b.do_full + 8 * sd;
             ptx::mbar_arrive_expect_tx(full, L::kTileBytes);
@@ -442,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the same unit (overlaps the gradient warps' dS(gi)), dK(gi), dQ(gi).
       auto issue_s = [&](int64_t g) -> bool {
         const int sq = static_cast<int>(g % L::kQStages);
-        if (!wait_warp(b.q_full + 8 * sq, static_cast<uint32_t>((g / L::kQStages) & 1), ctl, kSQFull)) return false;
+        if (!wait_warp<kProbe>(b.q_full + 8 * sq, static_cast<uint32_t>((g / L::kQStages) & 1), ctl, kSQFull)) return false;
         ptx::tc_fence_after();
         if (issuer) issue_kk(tmem + L::kColS, dK_k, dQ_k + sq * kTileUnits);
         if (leader) ptx::mma_commit(b.s_full);
@@ -451,13 +453,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       int64_t gi = 0, ku = 0;
       bool ok = true;
-      if (p.test_stall && blockIdx.x == 0) ok = wait_warp(b.never, 0, ctl, kSTest);
+      if (p.test_stall && blockIdx.x == 0) ok = wait_warp<kProbe>(b.never, 0, ctl, kSTest);
       for (int64_t k = 0; ok; ++k) {
         const int64_t u = unit_of(k, cta, grid);
         if (u >= p.n_units) break;
         const BUnit w = decode_bunit(p, ch, u);
         if (w.nit <= 0) continue;
-        if (!(ok = wait_warp(b.kv_full, static_cast<uint32_t>(ku & 1), ctl, kSKvFull))) break;
+        if (!(ok = wait_warp<kProbe>(b.kv_full, static_cast<uint32_t>(ku & 1), ctl, kSKvFull))) break;
         if (!(ok = issue_s(gi))) break;
         for (int it = 0; it < w.nit; ++it, ++gi) {
           const bool first = (it == 0);
@@ -466,16 +468,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t phd = static_cast<uint32_t>((gi / L::kDoStages) & 1);
           const uint32_t prev = static_cast<uint32_t>((gi - 1) & 1);
           const uint32_t cur = static_cast<uint32_t>(gi & 1);
-          if (!(ok = wait_warp(b.do_full + 8 * sd, phd, ctl, kSDoFull))) break;
+          if (!(ok = wait_warp<kProbe>(b.do_full + 8 * sd, phd, ctl, kSDoFull))) break;
           // D = 128: the previous dQ sits in the dP^T columns until the reduction warps read it
-          if (D == 128 && gi > 0 && !(ok = wait_warp(b.dq_free, prev, ctl, kSDqFree))) break;
+          if (D == 128 && gi > 0 && !(ok = wait_warp<kProbe>(b.dq_free, prev, ctl, kSDqFree))) break;
           ptx::tc_fence_after();
           if (issuer) issue_kk(tmem + L::kColDP, dV_k, dDO_k + sd * kTileUnits);
           if (leader) ptx::mma_commit(b.dp_full);
           __syncwarp();
-          if (!(ok = wait_warp(b.p_ready, cur, ctl, kSPReady))) break;
+          if (!(ok = wait_warp<kProbe>(b.p_ready, cur, ctl, kSPReady))) break;
           // the unit's first dV overwrites the accumulators: the previous unit's must be read out
-          if (first && ku > 0 && !(ok = wait_warp(b.acc_empty, static_cast<uint32_t>((ku - 1) & 1), ctl, kSAccEmpty)))
+          if (first && ku > 0 && !(ok = wait_warp<kProbe>(b.acc_empty, static_cast<uint32_t>((ku - 1) & 1), ctl, kSAccEmpty)))
             break;
           ptx::tc_fence_after();
           if (issuer) issue_ts(tmem + L::kColDV, tmem + L::kColS, dDO_mn + sd * kTileUnits, !first);
@@ -483,11 +485,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           // the next S^T may overwrite P^T: the dV product just issued reads it first (issue order)
           if (it + 1 < w.nit && !(ok = issue_s(gi + 1))) break;
-          if (!(ok = wait_warp(b.ds_ready, cur, ctl, kSDsReady))) break;
+          if (!(ok = wait_warp<kProbe>(b.ds_ready, cur, ctl, kSDsReady))) break;
           ptx::tc_fence_after();
           if (issuer) issue_ts(tmem + L::kColDK, tmem + L::kColDP, dQ_mn + st * kTileUnits, !first);
           __syncwarp();
-          if (D == 64 && gi > 0 && !(ok = wait_warp(b.dq_free, prev, ctl, kSDqFree))) break;
+          if (D == 64 && gi > 0 && !(ok = wait_warp<kProbe>(b.dq_free, prev, ctl, kSDqFree))) break;
           ptx::tc_fence_after();
           if (issuer) issue_dq(tmem + L::kColDQ);
           if (leader) {
@@ -548,8 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a_nl = sAux + st * 1024;  // -LSE*log2(e) of the tile's 128 rows
         const uint32_t a_nd = a_nl + 512;        // -D
         // the per-row runs were copied by the bulk engine: observe their barrier directly
-        if (!(ok = wait_warp(b.q_full + 8 * st, static_cast<uint32_t>((gi / L::kQStages) & 1), ctl, kSQFull))) break;
-        if (!(ok = wait_warp(b.s_full, cur, ctl, kSSFull))) break;
+        if (!(ok = wait_warp<kProbe>(b.q_full + 8 * st, static_cast<uint32_t>((gi / L::kQStages) & 1), ctl, kSQFull))) break;
+        if (!(ok = wait_warp<kProbe>(b.s_full, cur, ctl, kSSFull))) break;
         ptx::tc_fence_after();
         // all 128 columns of S^T in one go (one wait), then P in place
         uint32_t pf[4][32];
@@ -591,9 +593,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(b.p_ready);
 
-        if (!(ok = wait_warp(b.dp_full, cur, ctl, kSDpFull))) break;
+        if (!(ok = wait_warp<kProbe>(b.dp_full, cur, ctl, kSDpFull))) break;
         // the dS buffer in shared memory is free once the previous dQ product has read it
-        if (gi > 0 && !(ok = wait_warp(b.dq_full, static_cast<uint32_t>((gi - 1) & 1), ctl, kSDqFull))) break;
+        if (gi > 0 && !(ok = wait_warp<kProbe>(b.dq_full, static_cast<uint32_t>((gi - 1) & 1), ctl, kSDqFull))) break;
         ptx::tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -652,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (w.nit <= 0) continue;
       for (int it = 0; it < w.nit; ++it, ++gi) {
         const int t = w.t0 + it;
-        if (!(ok = wait_warp(b.dq_full, static_cast<uint32_t>(gi & 1), ctl, kSDqFull))) break;
+        if (!(ok = wait_warp<kProbe>(b.dq_full, static_cast<uint32_t>(gi & 1), ctl, kSDqFull))) break;
         ptx::tc_fence_after();
         // all of dQ into registers first, so the tensor memory goes back to the MMA warp (which
         // at D = 128 puts the next dP^T there) before any reduction is issued
@@ -670,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // end of the unit: dK (scaled) and dV
-      if (!(ok = wait_warp(b.acc_full, static_cast<uint32_t>(ku & 1), ctl, kSAccFull))) break;
+      if (!(ok = wait_warp<kProbe>(b.acc_full, static_cast<uint32_t>(ku & 1), ctl, kSAccFull))) break;
       ptx::tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {

@@ -24,9 +24,12 @@ __device__ __forceinline__ void raise_abort(const Ctl& c, int site) {
 }
 
 // Waits for phase `parity` of `bar`; false when the kernel is aborting or the limit expired (in
-// which case this wait starts the abort).
+// which case this wait starts the abort).  kProbe: test the phase once with the non-suspending
+// test_wait before the try_wait loop.  Without the probe the attention forward is 1.5-6.5 %
+// faster (same-box A/B); the D = 64 backward is 1.2 % faster with it.
+template <bool kProbe = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Ctl& c, int site) {
-  if (ptx::mbar_test_wait(bar, parity)) return true;
+  if (kProbe && ptx::mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
@@ -41,8 +44,9 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
 }
 
 // Every lane of the warp waits; the outcome is the same for the whole warp.
+template <bool kProbe = false>
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const Ctl& c, int site) {
-  const bool ok = wait_bounded(bar, parity, c, site);
+  const bool ok = wait_bounded<kProbe>(bar, parity, c, site);
   return __all_sync(0xffffffffu, ok);
 }
 
