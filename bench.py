@@ -568,13 +568,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def _profile_traffic(kernel_file, workload_key):
+KERNEL_SOURCES = ["attn_tc.cu", "ptx.cuh", "sync.cuh"]  # the forward kernel and the headers it includes
+
+
+def kernel_source_hash():
+    """sha256[:16] over the forward kernel's source and its own headers, in order."""
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "context_blockwise_attention_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _profile_traffic(workload_key):
     """DRAM bytes per launch of the dominant kernel from the committed ncu summary, or None when
     the kernel source changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "attn_tc_kernel_traffic.txt")
     try:
-        with open(kernel_file, "rb") as f:
-            h = hashlib.sha256(f.read()).hexdigest()[:16]
+        h = kernel_source_hash()
         with open(path) as f:
             for line in f:
                 parts = line.split()
@@ -777,8 +788,7 @@ def measure(cfg, layout, dev, world, local, steps, warmup, flush, *, fused_path=
                     "peak_source": f"derived: {sms} SMs x 128 FFMA/clk x 2 x {mhz:.0f} MHz",
                     "launches_per_step": len(step.attn_calls) + len(step.fused_calls), "traffic": None}
     else:
-        traffic = _profile_traffic(os.path.join(ROOT, "context_blockwise_attention_gb300", "csrc", "attn_tc.cu"),
-                                   f"cfg{cfg}" + ("_fused" if step.fused else ""))
+        traffic = _profile_traffic(f"cfg{cfg}" + ("_fused" if step.fused else ""))
         roofline = {"bound": "tensor", "kernel": "attn_tc_kernel", "achieved": achieved,
                     "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16"],
                     "peak_source": f"{peaks['source']} bf16 dense (burst)",
