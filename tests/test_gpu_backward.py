@@ -269,10 +269,12 @@ def test_ulysses_backward_three_steps_in_reverse():
         compare_grad(dvs[r].cpu().numpy(), dv_ref[sl], TOL_GRAD_BF16, f"Ulysses dV shard {r}")
 
 
-def test_bwd_bounded_wait_reports_timeout_and_context_survives():
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_bounded_wait_reports_timeout_and_context_survives(d):
     # block 0's MMA warp waits on a barrier nothing completes: its bounded wait expires, the
     # kernel records CP_ERR_TIMEOUT with the site, every CTA leaves, and the next call is correct
-    sq, skv, hq, hkv, d = 512, 512, 4, 2, 128
+    # (both head dims: their waits and MMA issue take different forms)
+    sq, skv, hq, hkv = 512, 512, 4, 2
     qm = km = PosMap(0, 1)
     q, k, v, d_o, o32, l32 = _case_inputs(sq, skv, hq, hkv, d, True, qm, km, torch.bfloat16, 9)
     aux = cpa.attn_bwd_prep(o32.to(DEV), d_o, l32.to(DEV))

@@ -270,8 +270,10 @@ def test_reshard_bit_exact(kind, dtype):
 
 # ------------------------------------------------------------------------------- fault
 
-def test_bounded_wait_reports_timeout_and_context_survives():
-    sq, skv, hq, hkv, d = 512, 512, 4, 2, 128
+@pytest.mark.parametrize("d", [64, 128])
+def test_bounded_wait_reports_timeout_and_context_survives(d):
+    # both head dims: the bounded waits and the MMA issue take a different form at each
+    sq, skv, hq, hkv = 512, 512, 4, 2
     q = wl.normal((sq, hq, d), torch.bfloat16, 1, device=DEV)
     k = wl.normal((skv, hkv, d), torch.bfloat16, 2, device=DEV)
     v = wl.normal((skv, hkv, d), torch.bfloat16, 3, device=DEV)
