@@ -349,3 +349,35 @@ def test_large_logits(d):
     ref = oracle.chunk_backward(q.cpu(), k1.cpu(), v1.cpu(), d_o.cpu(), o32, l32, qp, kp1, causal=True)
     for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
         compare_grad(g.cpu().numpy(), r, TOL_GRAD_BF16, f"large logits {name} d={d}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_score_jumps_inside_tiles(d):
+    """Every 128-key tile after the first raises the row maximum twice: keys 0..63 sit 7.9 (log2
+    units) above the previous tiles' maximum and keys 64..127 10.5 above it, each group with a
+    row sum of thousands, so the second half of a tile outgrows a reference that the first half
+    still fits and O and l are rescaled between the two halves' contributions.  Both halves carry
+    weight in the result (the first about a sixth of the second), so a contribution dropped or
+    scaled twice shows in O and LSE.  Checked against the oracle per chunk and over a chunk list."""
+    sq, hq, hkv, n = 1024, 2, 1, 1024
+    scale = 1.0 / np.sqrt(d)
+    u = np.full(d, 1.0 / np.sqrt(d))
+    level = np.zeros(n)
+    for t in range(1, n // 128):
+        base = 10.5 * (t - 1)
+        level[128 * t: 128 * t + 64] = base + 7.9
+        level[128 * t + 64: 128 * (t + 1)] = base + 10.5
+    a = level / (scale * np.log2(np.e))  # q = u, k_j = a_j u  =>  score_j * log2(e) = level_j
+    rng = np.random.default_rng(7)
+    q = torch.from_numpy(np.tile(u, (sq, hq, 1))).to(torch.bfloat16)
+    k = torch.from_numpy((a[:, None] * u[None, :])[:, None, :].repeat(hkv, axis=1)).to(torch.bfloat16)
+    v = torch.from_numpy(rng.standard_normal((n, hkv, d))).to(torch.bfloat16)
+    qm, km = PosMap(0, 1), PosMap(0, 1)
+    qp, kp = _pos(qm, sq), _pos(km, n)
+    ro, rl = oracle.attention(q, k, v, qp, kp, causal=True)
+    o, lse = cpa.partial_attn(q.to(DEV), k.to(DEV), v.to(DEV), qm, km, causal=True)
+    compare_partial(o.cpu().numpy(), lse.cpu().numpy(), ro, rl, TOL_BF16_O, TOL_BF16_LSE, f"score jumps d={d}")
+    half = n // 2
+    chunks = [(k[:half].to(DEV), v[:half].to(DEV), PosMap(0, 1)), (k[half:].to(DEV), v[half:].to(DEV), PosMap(half, 1))]
+    o2, l2 = cpa.partial_attn_chunks(q.to(DEV), chunks, qm, causal=True)
+    compare_partial(o2.cpu().numpy(), l2.cpu().numpy(), ro, rl, TOL_BF16_O, TOL_BF16_LSE, f"score jumps chunks d={d}")
